@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the MXFP4 lightning-indexer path on one GB300.
+
+One step is the whole decode hot path over one batch of 64 sequences with
+contexts uniform in [8K, 32K] (H = 32 index heads, head_dim 128, page 64,
+next_n = 1, top-k 2048; 1% outlier channels x8 in K and q):
+  1. quantise and insert the step's new key of every sequence (idx_quant_insert),
+  2. quantise the step's query heads (idx_quant_q),
+  3. paged MQA logits + top-k 2048 of every row, fused (idx_paged_logits_topk).
+The cache holds the rest of every context before timing starts.
+
+The metric is key-tokens scored per second (sum over query rows of the keys
+in the row's window, per second of step time) with the algorithmic HBM GB/s
+beside it.  L2 is flushed (a 256 MiB memset) before every timed step and each
+step is timed alone with CUDA events on the launching stream.
+
+--impl reference times the CPU oracle (the plain fp64 statement of the same
+path) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode K-tokens scored/s + HBM GB/s (paged MXFP4 MQA logits + top-k)"
+UNIT = "key-tokens/s"
+TOPK = 2048
+L2_FLUSH_BYTES = 256 << 20
+FUSED_SOURCES = ["paged_topk.cu", "paged_core.cuh", "topk_select.cuh", "common.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    return ap.parse_args()
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def workload_config(p):
+    return {"workload": "batched_decode", "sequences": p.B,
+            "context_lens": "uniform [8192, 32768]", "H": p.H, "head_dim": 128,
+            "page_size": 64, "next_n": p.next_n, "topk": p.topk,
+            "outliers": "1% channels x8 in K and q",
+            "scored_key_tokens_per_step": int(scored_tokens(p)),
+            "l2": "flushed before every timed step (256 MiB memset)"}
+
+
+def scored_tokens(p) -> int:
+    st, en = p.row_windows()
+    return int((en.astype(np.int64) - st).sum())
+
+
+def fused_algorithmic_bytes(p) -> int:
+    """Bytes the fused kernel must move: every cached key of every sequence
+    (64 value + 4 scale bytes), the block-table entries for those pages, the
+    context lengths, the query pairs and weights, and the top-k output."""
+    L = p.context_lens.astype(np.int64)
+    return int((68 * L + 4 * ((L + 63) // 64) + 4).sum() + p.rows * p.H * (68 + 4)
+               + p.rows * p.topk * 4)
+
+
+def step_algorithmic_bytes(p) -> int:
+    n_new = len(p.new_token_rows())
+    insert = n_new * (256 + 8 + 68)
+    qquant = p.rows * p.H * (256 + 68)
+    return fused_algorithmic_bytes(p) + insert + qquant
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_quant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "fused_decode_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha256") != source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bf16_tensor(a, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from sparse_attention_indexer_quant_gb300 import binding as idx
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    idx.check_device(local_rank)
+    p = wl.batched_decode(seed=1002 + 1000 * rank)
+    new_rows = p.new_token_rows()
+    old_mask = np.ones(p.total_tokens, bool)
+    old_mask[new_rows] = False
+
+    # resident state: the cache with every context except the newest token
+    cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+    k_old = bf16_tensor(p.k[old_mask], dev)
+    idx.quant_insert(k_old, torch.from_numpy(p.slots[old_mask]).to(dev), cache)
+    del k_old
+    new_k = bf16_tensor(p.k[new_rows], dev)
+    new_slots = torch.from_numpy(p.slots[new_rows]).to(dev)
+    q = bf16_tensor(p.q, dev)
+    w = torch.from_numpy(p.weights).to(dev)
+    bt = torch.from_numpy(p.block_table).to(dev)
+    cl = torch.from_numpy(p.context_lens).to(dev)
+    max_blocks = p.block_table.shape[1]
+    ws = idx.new_paged_topk_workspace(p.B, p.next_n, max_blocks, TOPK, dev)
+    qv = torch.empty((p.rows * p.H, 64), dtype=torch.uint8, device=dev)
+    qs = torch.empty((p.rows * p.H, 4), dtype=torch.uint8, device=dev)
+    out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        idx.quant_insert(new_k, new_slots, cache)
+        idx.quant_q(q, out_vals=qv, out_scales=qs)
+
+    def fused():
+        idx.paged_logits_topk(qv, qs, w, cache, bt, cl, p.next_n, p.H, TOPK, workspace=ws,
+                              out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+        fused()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            fused()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    fused_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    total_ms_max = reduce_max(total_ms, world, dev)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_new_k = bf16_tensor(p.k[new_rows], "cpu").pin_memory()
+    h_new_slots = pin(p.slots[new_rows])
+    h_q = bf16_tensor(p.q, "cpu").pin_memory()
+    h_w, h_bt, h_cl = pin(p.weights), pin(p.block_table), pin(p.context_lens)
+    h_out = torch.empty((p.rows, TOPK), dtype=torch.int32).pin_memory()
+    d_new_k, d_new_slots = torch.empty_like(new_k), torch.empty_like(new_slots)
+    d_q, d_w, d_bt, d_cl = (torch.empty_like(q), torch.empty_like(w), torch.empty_like(bt),
+                            torch.empty_like(cl))
+    h2d = sum(t.numel() * t.element_size() for t in (h_new_k, h_new_slots, h_q, h_w, h_bt, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_new_k, h_new_k), (d_new_slots, h_new_slots), (d_q, h_q), (d_w, h_w),
+                     (d_bt, h_bt), (d_cl, h_cl)):
+            d.copy_(h, non_blocking=True)
+        idx.quant_insert(d_new_k, d_new_slots, cache)
+        idx.quant_q(d_q, out_vals=qv, out_scales=qs)
+        idx.paged_logits_topk(qv, qs, d_w, cache, d_bt, d_cl, p.next_n, p.H, TOPK,
+                              workspace=ws, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_mean = reduce_max(sum(e2e_ms) / len(e2e_ms), world, dev)
+    # correctness spot check of the last e2e result against the device result
+    assert torch.equal(h_out, out.cpu())
+
+    cpu = None
+    if rank == 0:
+        cpu = cpu_baseline(p, args.cpu_sample_seqs)
+
+    if rank != 0:
+        return
+    tokens = scored_tokens(p) * world
+    ms_per_step = total_ms_max / K
+    value = tokens / (ms_per_step * 1e-3)
+    hbm_gbs = step_algorithmic_bytes(p) * world / (ms_per_step * 1e-3) / 1e9
+    fused_mean = sum(fused_ms) / K
+    achieved = fused_algorithmic_bytes(p) / (fused_mean * 1e-3) / 1e9
+    peak, peak_src = peaks()
+    traffic = measured_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, fp32 accumulate)",
+        "data": "synthetic (seeded bf16 N(0,1) keys/queries, shuffled block tables)",
+        "config": workload_config(p),
+        "hbm_gbs": hbm_gbs,
+        "fused_kernel_ms": fused_mean,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": f"paged_topk_kernel<H={p.H},next_n={p.next_n}>",
+                     "peak_source": f"{peak_src} (hbm_gbs, burst)",
+                     "algorithmic_bytes_per_launch": fused_algorithmic_bytes(p)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": scored_tokens(p) * world / (e2e_mean * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_mean},
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(p, n_seq):
+    """The oracle, as it stands, on the first n_seq sequences of the batch:
+    insert of their new keys, query quantisation, paged logits and top-k."""
+    import oracle
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    n_seq = max(1, min(n_seq, p.B))
+    hi_tok = int(p.tok_offsets[n_seq])
+    cache = wl.poisoned_cache(p.num_blocks)
+    new_rows = [r for r in p.new_token_rows() if r < hi_tok]
+    old = np.setdiff1d(np.arange(hi_tok), new_rows)
+    oracle.quant_insert(p.k[old], p.slots[old], cache)
+    rows = n_seq * p.next_n
+    t0 = time.perf_counter()
+    oracle.quant_insert(p.k[new_rows], p.slots[new_rows], cache)
+    qv, qs = oracle.quant_q(p.q[:rows])
+    ld = p.block_table.shape[1] * 64
+    lg, _ = oracle.paged_mqa_logits(qv, qs, n_seq, p.next_n, p.H, cache, p.block_table[:n_seq],
+                                    p.context_lens[:n_seq], p.weights[:rows], ld)
+    st, en = p.row_windows()
+    oracle.topk_rows(np.nan_to_num(lg, nan=-np.inf), st[:rows], en[:rows], p.topk)
+    dt = time.perf_counter() - t0
+    toks = int((en[:rows].astype(np.int64) - st[:rows]).sum())
+    return {"value": toks / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {n_seq} of {p.B} sequences ({toks} key-tokens), one decode step",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is the oracle's decode step
+    over a bounded sample of the workload's sequences."""
+    if rank != 0:
+        return
+    import oracle
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    p = wl.batched_decode()
+    # calibrate the per-step sample so that warmup + steps take about 90 s
+    budget_s = 90.0
+    n_steps = args.steps + args.warmup
+    probe = cpu_baseline(p, 1)
+    rate = probe["value"]
+    per_step_tokens = max(2048, int(rate * budget_s / max(n_steps, 1)))
+    # sample: the first sequences whose windows fit per_step_tokens; a window may
+    # be cut short to fit (the rate is per key-token)
+    lens = p.context_lens.astype(np.int64)
+    n_seq = int(np.searchsorted(np.cumsum(lens), per_step_tokens, side="right"))
+    n_seq = max(1, min(n_seq, p.B))
+    cut = min(int(lens[:n_seq].sum()), per_step_tokens)
+    cache = wl.poisoned_cache(p.num_blocks)
+    hi_tok = int(p.tok_offsets[n_seq])
+    oracle.quant_insert(p.k[:hi_tok], p.slots[:hi_tok], cache)
+    ctx = p.context_lens[:n_seq].copy()
+    over = int(ctx.astype(np.int64).sum()) - cut
+    if over > 0:
+        ctx[-1] = max(1, int(ctx[-1]) - over)
+    rows = n_seq * p.next_n
+    new_rows = [r for r in p.new_token_rows() if r < hi_tok]
+    ld = p.block_table.shape[1] * 64
+
+    def one():
+        oracle.quant_insert(p.k[new_rows], p.slots[new_rows], cache)
+        qv, qs = oracle.quant_q(p.q[:rows])
+        lg, _ = oracle.paged_mqa_logits(qv, qs, n_seq, p.next_n, p.H, cache,
+                                        p.block_table[:n_seq], ctx, p.weights[:rows], ld)
+        en = ctx.astype(np.int32)
+        oracle.topk_rows(np.nan_to_num(lg, nan=-np.inf), np.zeros_like(en), en, p.topk)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    toks = int(ctx.astype(np.int64).sum())
+    value = toks * args.steps / dt
+    sample = (f"first {n_seq} of {p.B} sequences, {toks} key-tokens per step "
+              f"(oracle decode step: insert, q-quant, logits, top-k)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": workload_config(p),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+_PG = None
+
+
+def init_dist(world):
+    global _PG
+    if world <= 1:
+        return
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        backend = "nccl" if __import__("torch").cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    _PG = dist
+
+
+def barrier(world):
+    if world > 1 and _PG is not None:
+        _PG.barrier()
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Largest value of x over the ranks (the whole job ends with its slowest rank)."""
+    if world <= 1 or _PG is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    _PG.all_reduce(t, op=_PG.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_info()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    init_dist(world)
+    run_ours(args, rank, world, local_rank)
+    if world > 1 and _PG is not None:
+        _PG.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

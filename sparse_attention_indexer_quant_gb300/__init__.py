@@ -4,11 +4,16 @@ The compute lives in ``libidx.so`` (hand-written sm_103a CUDA behind a C ABI,
 declared in ``include/idx.h``); ``binding`` marshals PyTorch tensors to it.
 ``workloads`` draws seeded synthetic inputs and needs no GPU.
 """
-from . import workloads  # noqa: F401
+import importlib
+
+_SUBMODULES = {"binding", "build_lib", "workloads"}
 
 
 def __getattr__(name):
-    # The binding loads the CUDA library; import it only when an op is used so
-    # that the CPU-only parts of the package import without it.
-    from . import binding
-    return getattr(binding, name)
+    # The binding loads the CUDA library; it is imported only when an op is
+    # used, so that the CPU-only parts of the package import without it.
+    if name in _SUBMODULES:
+        return importlib.import_module(f".{name}", __name__)
+    if name.startswith("__"):
+        raise AttributeError(name)
+    return getattr(importlib.import_module(".binding", __name__), name)

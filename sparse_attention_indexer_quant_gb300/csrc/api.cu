@@ -1,0 +1,358 @@
+// C ABI of libidx (declared in include/idx.h): argument validation, the
+// fail-closed architecture gate, TMA tensor-map encoding and kernel dispatch.
+// Nothing here allocates device memory or synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "idx.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_detail[512] = "";
+
+idx_status fail(idx_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+idx_status ok() {
+  g_detail[0] = '\0';
+  return IDX_OK;
+}
+
+idx_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(IDX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- device gate, cached per device
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 rejected
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+idx_status current_device_ok(int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(IDX_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+  int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return from_cuda(e, "cudaDeviceGetAttribute");
+    st = idx_arch_supported(major, minor) == IDX_OK ? 1 : 2;
+    g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+    g_dev_state[dev].store(st, std::memory_order_release);
+  }
+  if (st != 1)
+    return fail(IDX_ERR_UNSUPPORTED_DEVICE, "device %d is not sm_103 (GB300); refusing", dev);
+  if (sms_out) *sms_out = g_dev_sms[dev].load(std::memory_order_relaxed);
+  return IDX_OK;
+}
+
+// ---- tensor maps through the driver entry point (no link-time libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Value area of the paged cache: 3-D (64 bytes, 64 rows, num_blocks) with
+// strides (64, 4352), one page per box, 64-byte swizzle.
+idx_status cache_value_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[3] = {64, 64, (cuuint64_t)num_blocks};
+  const cuuint64_t strides[2] = {64, (cuuint64_t)idx::kPageBytes};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(cache), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (cache values): CUresult %d", (int)r);
+  return IDX_OK;
+}
+
+// Scale area of the paged cache: 2-D (256 bytes, num_blocks), stride 4352.
+idx_status cache_scale_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {256, (cuuint64_t)num_blocks};
+  const cuuint64_t strides[1] = {(cuuint64_t)idx::kPageBytes};
+  const cuuint32_t box[2] = {256, 1};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<uint8_t*>(cache + idx::kPageValBytes), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (cache scales): CUresult %d", (int)r);
+  return IDX_OK;
+}
+
+idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
+                              int32_t next_n, int32_t H, const uint8_t* kcache,
+                              int64_t num_blocks, int32_t page_size, const int32_t* block_table,
+                              int32_t max_blocks, const int32_t* context_lens,
+                              const float* weights) {
+  if (B < 0 || B > 65535) return fail(IDX_ERR_INVALID_ARG, "B=%d outside [0, 65535]", B);
+  if (next_n != 1 && next_n != 2) return fail(IDX_ERR_INVALID_ARG, "next_n=%d not in {1,2}", next_n);
+  if (H != 32 && H != 64) return fail(IDX_ERR_INVALID_ARG, "H=%d not in {32,64}", H);
+  if (page_size != 64) return fail(IDX_ERR_INVALID_ARG, "page_size=%d (only 64)", page_size);
+  if (max_blocks <= 0 || max_blocks > (1 << 24))
+    return fail(IDX_ERR_INVALID_ARG, "max_blocks=%d", max_blocks);
+  if (num_blocks <= 0 || num_blocks > (int64_t)INT32_MAX)
+    return fail(IDX_ERR_INVALID_ARG, "num_blocks=%lld", (long long)num_blocks);
+  if (B == 0) return IDX_OK;
+  if (!q_vals || !q_scales || !kcache || !block_table || !context_lens || !weights)
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_vals, 16) || !aligned(kcache, 16) || !aligned(q_scales, 4) ||
+      !aligned(weights, 16))
+    return fail(IDX_ERR_INVALID_ARG,
+                "alignment: q_vals/kcache/weights need 16 bytes, q_scales 4 bytes");
+  return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int idx_version(void) { return 100; }
+
+const char* idx_status_string(idx_status s) {
+  switch (s) {
+    case IDX_OK: return "ok";
+    case IDX_ERR_INVALID_ARG: return "invalid argument";
+    case IDX_ERR_UNSUPPORTED_DEVICE: return "unsupported device (sm_103 required)";
+    case IDX_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case IDX_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char* idx_last_error_detail(void) { return g_detail; }
+
+idx_status idx_arch_supported(int major, int minor) {
+  return (major == 10 && minor == 3) ? IDX_OK : IDX_ERR_UNSUPPORTED_DEVICE;
+}
+
+idx_status idx_check_device(int device) {
+  int major = 0, minor = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  if (e != cudaSuccess) return from_cuda(e, "cudaDeviceGetAttribute");
+  idx_status s = idx_arch_supported(major, minor);
+  if (s != IDX_OK) return fail(s, "device %d has compute capability %d.%d", device, major, minor);
+  return ok();
+}
+
+idx_status idx_quant_insert(const void* k_bf16, int64_t n_tokens, int64_t k_row_stride,
+                            const int64_t* slot_mapping, uint8_t* kcache, int64_t num_blocks,
+                            int32_t page_size, idx_device_errors* errors, idx_stream_t stream) {
+  if (n_tokens < 0 || n_tokens > (int64_t)INT32_MAX * 16)
+    return fail(IDX_ERR_INVALID_ARG, "n_tokens=%lld", (long long)n_tokens);
+  if (page_size != 64) return fail(IDX_ERR_INVALID_ARG, "page_size=%d (only 64)", page_size);
+  if (num_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "num_blocks=%lld", (long long)num_blocks);
+  if (k_row_stride < 128 || (k_row_stride % 8) != 0)
+    return fail(IDX_ERR_INVALID_ARG, "k_row_stride=%lld (>= 128, multiple of 8)",
+                (long long)k_row_stride);
+  idx_status s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (n_tokens == 0) return ok();
+  if (!k_bf16 || !slot_mapping || !kcache) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k_bf16, 16) || !aligned(kcache, 16) || !aligned(slot_mapping, 8))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: k_bf16/kcache need 16 bytes, slots 8");
+  return from_cuda(idx::launch_quant_insert(k_bf16, n_tokens, k_row_stride, slot_mapping, kcache,
+                                            num_blocks, errors, (cudaStream_t)stream),
+                   "quant_insert launch");
+}
+
+idx_status idx_quant_q(const void* q_bf16, int64_t rows, uint8_t* q_vals, uint8_t* q_scales,
+                       idx_stream_t stream) {
+  if (rows < 0 || rows > (int64_t)INT32_MAX * 16)
+    return fail(IDX_ERR_INVALID_ARG, "rows=%lld", (long long)rows);
+  idx_status s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (rows == 0) return ok();
+  if (!q_bf16 || !q_vals || !q_scales) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_bf16, 16) || !aligned(q_vals, 4) || !aligned(q_scales, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: q_bf16 16 bytes, outputs 4 bytes");
+  return from_cuda(idx::launch_quant_q(q_bf16, rows, q_vals, q_scales, (cudaStream_t)stream),
+                   "quant_q launch");
+}
+
+idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
+                                int32_t next_n, int32_t H, const uint8_t* kcache,
+                                int64_t num_blocks, int32_t page_size,
+                                const int32_t* block_table, int32_t max_blocks,
+                                const int32_t* context_lens, const float* weights,
+                                float* logits, int64_t ld, int clean, idx_device_errors* errors,
+                                idx_stream_t stream) {
+  idx_status s = check_paged_common(q_vals, q_scales, B, next_n, H, kcache, num_blocks, page_size,
+                                    block_table, max_blocks, context_lens, weights);
+  if (s != IDX_OK) return s;
+  if (ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld", (long long)ld);
+  int sms = 0;
+  s = current_device_ok(&sms);
+  if (s != IDX_OK) return s;
+  if (B == 0) return ok();
+  if (!logits) return fail(IDX_ERR_INVALID_ARG, "null logits");
+  CUtensorMap tv, ts;
+  if ((s = cache_value_map(&tv, kcache, num_blocks)) != IDX_OK) return s;
+  if ((s = cache_scale_map(&ts, kcache, num_blocks)) != IDX_OK) return s;
+  idx::PagedArgs a{};
+  a.q_vals = q_vals;
+  a.q_scales = q_scales;
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.weights = weights;
+  a.logits = logits;
+  a.ld = ld;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.max_blocks = max_blocks;
+  a.clean = clean ? 1 : 0;
+  a.errors = errors;
+  const int64_t cap = (int64_t)max_blocks * 64;
+  const int64_t cols = a.clean ? ld : (ld < cap ? ld : cap);
+  const int64_t tiles = (cols + 127) / 128;
+  // about four CTAs per SM over the whole batch, 2..64 tiles each
+  int64_t per = (tiles * B + 4LL * sms - 1) / (4LL * sms);
+  per = per < 2 ? 2 : (per > 64 ? 64 : per);
+  a.tiles_per_cta = (int32_t)per;
+  const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
+  if (chunks > INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "ld too large");
+  a.chunks = (int32_t)chunks;
+  return from_cuda(idx::launch_paged_logits(tv, ts, H, next_n, a, (cudaStream_t)stream),
+                   "paged_mqa_logits launch");
+}
+
+idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int64_t T, int32_t H,
+                          const uint8_t* k_vals, const uint8_t* k_scales, int64_t S,
+                          const float* weights, const int32_t* row_start,
+                          const int32_t* row_end, float* logits, int64_t ld, int clean,
+                          idx_stream_t stream) {
+  (void)q_vals; (void)q_scales; (void)T; (void)H; (void)k_vals; (void)k_scales; (void)S;
+  (void)weights; (void)row_start; (void)row_end; (void)logits; (void)ld; (void)clean;
+  (void)stream;
+  return fail(IDX_ERR_INVALID_ARG, "idx_mqa_logits: not available in this build");
+}
+
+idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const int32_t* row_start,
+                         const int32_t* row_end, int32_t k, int32_t* out_idx,
+                         idx_stream_t stream) {
+  if (rows < 0 || rows > (int64_t)INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "rows=%lld", (long long)rows);
+  if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
+  if (ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld", (long long)ld);
+  idx_status s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (rows == 0) return ok();
+  if (!logits || !row_end || !out_idx) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  return from_cuda(idx::launch_topk_rows(logits, rows, ld, row_start, row_end, k, out_idx,
+                                         (cudaStream_t)stream),
+                   "topk_rows launch");
+}
+
+size_t idx_paged_logits_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks,
+                                             int32_t page_size, int32_t k) {
+  (void)page_size;
+  return idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, nullptr, nullptr);
+}
+
+idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
+                                 int32_t next_n, int32_t H, const uint8_t* kcache,
+                                 int64_t num_blocks, int32_t page_size,
+                                 const int32_t* block_table, int32_t max_blocks,
+                                 const int32_t* context_lens, const float* weights, int32_t k,
+                                 int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                                 idx_device_errors* errors, idx_stream_t stream) {
+  idx_status s = check_paged_common(q_vals, q_scales, B, next_n, H, kcache, num_blocks, page_size,
+                                    block_table, max_blocks, context_lens, weights);
+  if (s != IDX_OK) return s;
+  if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
+  s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (B == 0) return ok();
+  if (!out_idx) return fail(IDX_ERR_INVALID_ARG, "null out_idx");
+  int32_t per = 0, chunks = 0;
+  const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, &per, &chunks);
+  if (workspace_bytes < need || workspace == nullptr)
+    return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  CUtensorMap tv, ts;
+  if ((s = cache_value_map(&tv, kcache, num_blocks)) != IDX_OK) return s;
+  if ((s = cache_scale_map(&ts, kcache, num_blocks)) != IDX_OK) return s;
+  idx::PagedArgs a{};
+  a.q_vals = q_vals;
+  a.q_scales = q_scales;
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.weights = weights;
+  a.logits = nullptr;
+  a.ld = 0;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.max_blocks = max_blocks;
+  a.clean = 0;
+  a.tiles_per_cta = per;
+  a.chunks = chunks;
+  a.topk = k;
+  a.out_idx = out_idx;
+  a.workspace = workspace;
+  a.errors = errors;
+  return from_cuda(idx::launch_paged_logits_topk(tv, ts, H, next_n, a, (cudaStream_t)stream),
+                   "paged_logits_topk launch");
+}
+
+idx_status idx_gather_k(const uint8_t* kcache, int64_t num_blocks, int32_t page_size,
+                        const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                        const int64_t* out_offsets, int32_t B, uint8_t* k_vals,
+                        uint8_t* k_scales, int64_t out_rows, idx_device_errors* errors,
+                        idx_stream_t stream) {
+  if (B < 0 || B > 65535) return fail(IDX_ERR_INVALID_ARG, "B=%d outside [0, 65535]", B);
+  if (page_size != 64) return fail(IDX_ERR_INVALID_ARG, "page_size=%d (only 64)", page_size);
+  if (max_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks=%d", max_blocks);
+  if (num_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "num_blocks=%lld", (long long)num_blocks);
+  if (out_rows < 0) return fail(IDX_ERR_INVALID_ARG, "out_rows=%lld", (long long)out_rows);
+  idx_status s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (B == 0) return ok();
+  if (!kcache || !block_table || !seq_lens || !out_offsets || !k_vals || !k_scales)
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(kcache, 16) || !aligned(k_vals, 16) || !aligned(k_scales, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: kcache/k_vals 16 bytes, k_scales 4");
+  return from_cuda(idx::launch_gather_k(kcache, num_blocks, block_table, max_blocks, seq_lens,
+                                        out_offsets, B, k_vals, k_scales, out_rows, errors,
+                                        (cudaStream_t)stream),
+                   "gather_k launch");
+}
+
+}  // extern "C"

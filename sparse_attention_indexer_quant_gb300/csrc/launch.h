@@ -1,0 +1,77 @@
+// Internal launchers behind the C ABI (argument checking happens in api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "idx.h"
+
+namespace idx {
+
+cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_stride,
+                                const int64_t* slots, uint8_t* cache, int64_t num_blocks,
+                                idx_device_errors* errors, cudaStream_t stream);
+
+cudaError_t launch_quant_q(const void* q, int64_t rows, uint8_t* vals, uint8_t* scales,
+                           cudaStream_t stream);
+
+// Paged decode: tensor maps over the cache's value area (3-D: 64 B x 64 rows x
+// num_blocks, 64-byte swizzle) and scale area (2-D: 256 B x num_blocks).
+struct PagedArgs {
+  const uint8_t* q_vals;
+  const uint8_t* q_scales;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  const float* weights;
+  float* logits;          // unfused: [rows, ld]
+  int64_t ld;
+  int64_t num_blocks;
+  int32_t B;
+  int32_t max_blocks;
+  int32_t clean;
+  int32_t tiles_per_cta;  // keys per CTA = 128 * tiles_per_cta
+  int32_t chunks;         // CTAs per sequence
+  int32_t topk;           // fused only
+  int32_t* out_idx;       // fused only: [rows, topk]
+  void* workspace;        // fused only
+  idx_device_errors* errors;
+};
+
+cudaError_t launch_paged_logits(const CUtensorMap& tm_vals, const CUtensorMap& tm_scales,
+                                int H, int next_n, const PagedArgs& a, cudaStream_t stream);
+
+cudaError_t launch_paged_logits_topk(const CUtensorMap& tm_vals, const CUtensorMap& tm_scales,
+                                     int H, int next_n, const PagedArgs& a, cudaStream_t stream);
+size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k,
+                                  int32_t* tiles_per_cta_out, int32_t* chunks_out);
+
+// Prefill: tensor maps over contiguous keys (values 2-D: 64 B x S, 64-byte
+// swizzle; scales 2-D: 512 B x ceil(S/128) tiles).
+struct MqaArgs {
+  const uint8_t* q_vals;
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const float* weights;
+  const int32_t* row_start;
+  const int32_t* row_end;
+  float* logits;
+  int64_t T;
+  int64_t S;
+  int64_t ld;
+  int32_t clean;
+};
+cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs& a,
+                              cudaStream_t stream);
+
+cudaError_t launch_topk_rows(const float* logits, int64_t rows, int64_t ld,
+                             const int32_t* row_start, const int32_t* row_end, int32_t k,
+                             int32_t* out, cudaStream_t stream);
+
+cudaError_t launch_gather_k(const uint8_t* cache, int64_t num_blocks, const int32_t* block_table,
+                            int32_t max_blocks, const int32_t* seq_lens,
+                            const int64_t* out_offsets, int32_t B, uint8_t* k_vals,
+                            uint8_t* k_scales, int64_t out_rows, idx_device_errors* errors,
+                            cudaStream_t stream);
+
+}  // namespace idx

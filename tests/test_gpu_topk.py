@@ -1,0 +1,84 @@
+"""GPU parity of top-k per row against the oracle through the C ABI: ragged
+rows around k, rows with ties and all-equal rows, window offsets, k below
+2048, and the prefill-shaped causal case."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_indexer_quant_gb300 import workloads as wl
+from idx_testutil import check_topk, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def idx():
+    from sparse_attention_indexer_quant_gb300 import binding
+    binding.check_device(torch.cuda.current_device())
+    return binding
+
+
+def run(idx, logits32, starts, ends, k):
+    out = idx.topk_rows(dev(logits32), dev(ends.astype(np.int32)), k,
+                        row_start=dev(starts.astype(np.int32)))
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("k", [2048, 16, 1])
+def test_topk_random_rows(idx, k):
+    g = wl.rng(400 + k)
+    lens = np.array([0, 1, 5, k - 1 if k > 1 else 0, k, k + 1, 2 * k + 3, 5000, 40000, 131072])
+    starts = g.integers(0, 50, size=len(lens))
+    ld = int((starts + lens).max()) + 7
+    logits = np.full((len(lens), ld), np.nan, np.float32)
+    for r, (s, n) in enumerate(zip(starts, lens)):
+        logits[r, s:s + n] = g.standard_normal(n).astype(np.float32)
+    out = run(idx, logits, starts, starts + lens, k)
+    for r, (s, n) in enumerate(zip(starts, lens)):
+        vals = logits[r, s:s + n].astype(np.float64)
+        check_topk(out[r], vals, np.zeros_like(vals), int(n), k, f"row {r} len {n}")
+
+
+def test_topk_ties(idx):
+    """Few distinct values: the selected set must hold every index above the
+    k-th value and fill the rest with indices equal to it."""
+    g = wl.rng(410)
+    k = 2048
+    lens = np.array([3000, 10000, 70000])
+    ld = int(lens.max())
+    logits = np.full((3, ld), np.nan, np.float32)
+    for r, n in enumerate(lens):
+        logits[r, :n] = (g.integers(-3, 4, size=n) * 0.5).astype(np.float32)
+    out = run(idx, logits, np.zeros(3, np.int64), lens, k)
+    for r, n in enumerate(lens):
+        vals = logits[r, :n].astype(np.float64)
+        check_topk(out[r], vals, np.zeros_like(vals), int(n), k, f"ties row {r}")
+
+
+def test_topk_all_equal_and_neg_inf(idx):
+    k = 2048
+    n = 20000
+    logits = np.zeros((3, n), np.float32)
+    logits[1, :] = -np.inf
+    logits[1, 123] = 5.0
+    logits[2, :] = 1.0
+    logits[2, 5000:5010] = 2.0
+    out = run(idx, logits, np.zeros(3, np.int64), np.full(3, n), k)
+    for r in range(3):
+        vals = logits[r].astype(np.float64)
+        check_topk(out[r], vals, np.zeros_like(vals), n, k, f"row {r}")
+    assert 123 in out[1].tolist()
+    assert set(range(5000, 5010)) <= set(out[2].tolist())
+
+
+def test_topk_causal_prefill_rows(idx):
+    """Rows of a causal prefill: row t sees [0, t+1)."""
+    g = wl.rng(420)
+    T = 3000
+    logits = g.standard_normal((T, T)).astype(np.float32)
+    ends = np.arange(1, T + 1)
+    out = run(idx, logits, np.zeros(T, np.int64), ends, 2048)
+    for t in [0, 1, 2046, 2047, 2048, 2049, 2999]:
+        vals = logits[t, :t + 1].astype(np.float64)
+        check_topk(out[t], vals, np.zeros_like(vals), t + 1, 2048, f"t={t}")

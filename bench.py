@@ -50,7 +50,27 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--workload", default="batched_decode",
+                    choices=sorted(WORKLOADS),
+                    help="decode workload; the default is the headline configuration")
     return ap.parse_args()
+
+
+# decode workloads (the pages' shapes): name -> (builder name, description)
+WORKLOADS = {
+    "batched_decode": ("batched_decode", "64 sequences, contexts uniform [8192, 32768], H=32, next_n=1"),
+    "pr_ref": ("pr_ref", "1 sequence of 8192 tokens, H=32, next_n=1"),
+    "long_decode": ("long_decode", "16 sequences x 131072 tokens, H=64, next_n=2"),
+    "mixed_decode": ("mixed_decode_part", "128 sequences, contexts uniform [1024, 131072], H=32, next_n=1"),
+}
+
+
+def make_workload(name, rank=0):
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    builder = getattr(wl, WORKLOADS[name][0])
+    import inspect
+    seed = inspect.signature(builder).parameters["seed"].default
+    return builder(seed=seed + 1000 * rank)
 
 
 def dist_info():
@@ -58,11 +78,10 @@ def dist_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def workload_config(p):
-    return {"workload": "batched_decode", "sequences": p.B,
-            "context_lens": "uniform [8192, 32768]", "H": p.H, "head_dim": 128,
+def workload_config(p, name="batched_decode"):
+    return {"workload": name, "description": WORKLOADS[name][1], "sequences": p.B,
+            "H": p.H, "head_dim": 128,
             "page_size": 64, "next_n": p.next_n, "topk": p.topk,
-            "outliers": "1% channels x8 in K and q",
             "scored_key_tokens_per_step": int(scored_tokens(p)),
             "l2": "flushed before every timed step (256 MiB memset)"}
 
@@ -188,7 +207,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     idx.check_device(local_rank)
-    p = wl.batched_decode(seed=1002 + 1000 * rank)
+    p = make_workload(args.workload, rank)
     new_rows = p.new_token_rows()
     old_mask = np.ones(p.total_tokens, bool)
     old_mask[new_rows] = False
@@ -303,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, fp32 accumulate)",
         "data": "synthetic (seeded bf16 N(0,1) keys/queries, shuffled block tables)",
-        "config": workload_config(p),
+        "config": workload_config(p, args.workload),
         "hbm_gbs": hbm_gbs,
         "fused_kernel_ms": fused_mean,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -355,7 +374,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     from sparse_attention_indexer_quant_gb300 import workloads as wl
-    p = wl.batched_decode()
+    p = make_workload(args.workload)
     # calibrate the per-step sample so that warmup + steps take about 90 s
     budget_s = 90.0
     n_steps = args.steps + args.warmup
@@ -401,7 +420,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": workload_config(p),
+        "data": "synthetic (seeded)", "config": workload_config(p, args.workload),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -152,7 +152,8 @@ IDX_API idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_
  *   k_vals/k_scales  [S, 64] / [S, 4] (e.g. from idx_gather_k), 16-byte aligned.
  *   weights          [T, H] fp32.
  *   row_start/row_end [T] int32: query t sees keys [row_start[t], row_end[t]),
- *                    0 <= start <= end <= S.
+ *                    0 <= start <= end <= S (windows outside are clamped and
+ *                    counted in errors->bad_inputs).
  *   logits           [T, ld] fp32 out, ld >= S.  Columns in the window get the
  *                    logit; with clean != 0 the other columns of [0, S) get
  *                    -inf, otherwise they are not written.
@@ -161,7 +162,7 @@ IDX_API idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales
                           const uint8_t* k_vals, const uint8_t* k_scales, int64_t S,
                           const float* weights, const int32_t* row_start,
                           const int32_t* row_end, float* logits, int64_t ld, int clean,
-                          idx_stream_t stream);
+                          idx_device_errors* errors, idx_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * idx_topk_rows -- top-k per logits row (sparse_indexer docs: top_k_per_row

@@ -36,7 +36,7 @@ SIGNATURES = {
     "idx_paged_mqa_logits": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _I32, _P, _I32,
                                             _P, _P, _P, _I64, ctypes.c_int, _P, _P]),
     "idx_mqa_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _P, _I64, _P, _P, _P, _P, _I64,
-                                      ctypes.c_int, _P]),
+                                      ctypes.c_int, _P, _P]),
     "idx_topk_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I32, _P, _P]),
     "idx_paged_logits_topk_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "idx_paged_logits_topk": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _I32, _P, _I32,
@@ -203,7 +203,7 @@ def paged_logits_topk(q_vals, q_scales, weights, kcache, block_table, context_le
 
 
 def mqa_logits(q_vals, q_scales, weights, k_vals, k_scales, row_start, row_end, H: int,
-               ld: int | None = None, clean: bool = False, out=None, stream=None):
+               ld: int | None = None, clean: bool = False, out=None, errors=None, stream=None):
     _need(q_vals, torch.uint8, "q_vals")
     _need(q_scales, torch.uint8, "q_scales")
     _need(k_vals, torch.uint8, "k_vals")
@@ -219,7 +219,8 @@ def mqa_logits(q_vals, q_scales, weights, k_vals, k_scales, row_start, row_end, 
                                                      device=q_vals.device)
     _check("idx_mqa_logits", lib.idx_mqa_logits(
         _ptr(q_vals), _ptr(q_scales), T, H, _ptr(k_vals), _ptr(k_scales), S, _ptr(weights),
-        _ptr(row_start), _ptr(row_end), _ptr(logits), ld, 1 if clean else 0, _stream(stream)))
+        _ptr(row_start), _ptr(row_end), _ptr(logits), ld, 1 if clean else 0, _ptr(errors),
+        _stream(stream)))
     return logits
 
 

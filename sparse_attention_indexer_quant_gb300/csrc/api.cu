@@ -259,11 +259,44 @@ idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int64_
                           const uint8_t* k_vals, const uint8_t* k_scales, int64_t S,
                           const float* weights, const int32_t* row_start,
                           const int32_t* row_end, float* logits, int64_t ld, int clean,
-                          idx_stream_t stream) {
-  (void)q_vals; (void)q_scales; (void)T; (void)H; (void)k_vals; (void)k_scales; (void)S;
-  (void)weights; (void)row_start; (void)row_end; (void)logits; (void)ld; (void)clean;
-  (void)stream;
-  return fail(IDX_ERR_INVALID_ARG, "idx_mqa_logits: not available in this build");
+                          idx_device_errors* errors, idx_stream_t stream) {
+  if (T < 0 || T > (int64_t)INT32_MAX * 4) return fail(IDX_ERR_INVALID_ARG, "T=%lld", (long long)T);
+  if (H != 32 && H != 64) return fail(IDX_ERR_INVALID_ARG, "H=%d not in {32,64}", H);
+  if (S < 0 || S > (int64_t)INT32_MAX - 256) return fail(IDX_ERR_INVALID_ARG, "S=%lld", (long long)S);
+  if (ld < S || ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld < S=%lld", (long long)ld, (long long)S);
+  idx_status s = current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (T == 0 || S == 0) return ok();
+  if (!q_vals || !q_scales || !k_vals || !k_scales || !weights || !row_start || !row_end || !logits)
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_vals, 16) || !aligned(k_vals, 16) || !aligned(q_scales, 4) ||
+      !aligned(k_scales, 4) || !aligned(weights, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: q_vals/k_vals 16 bytes, scales/weights 4");
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  CUtensorMap tk;
+  const cuuint64_t dims[2] = {64, (cuuint64_t)S};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(k_vals), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (keys): CUresult %d", (int)r);
+  idx::MqaArgs a{};
+  a.q_vals = q_vals;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.weights = weights;
+  a.row_start = row_start;
+  a.row_end = row_end;
+  a.logits = logits;
+  a.T = T;
+  a.S = S;
+  a.ld = ld;
+  a.clean = clean ? 1 : 0;
+  a.errors = errors;
+  return from_cuda(idx::launch_mqa_logits(tk, H, a, (cudaStream_t)stream), "mqa_logits launch");
 }
 
 idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const int32_t* row_start,

@@ -60,6 +60,7 @@ struct MqaArgs {
   int64_t S;
   int64_t ld;
   int32_t clean;
+  idx_device_errors* errors;
 };
 cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs& a,
                               cudaStream_t stream);

@@ -1,0 +1,308 @@
+// Prefill MQA logits over contiguous MXFP4 keys (vLLM API docs
+// "vllm.models.glm5next.nvidia.sparse_indexer": mqa_logits; the keys come from
+// the gather of the block-split cache, vLLM PR #48558 "Live validation").
+//
+//     logit[t, s] = sum_h w[t, h] * max(0, q^[t, h] . k^[s]),  s in [start_t, end_t)
+//
+// One CTA per group of G = 256 / H query tokens: the group's G*H query heads
+// are the MMA's B operand (N = 256).  Keys stream through 128-key tiles from
+// the union of the group's windows:
+//   warp 0      TMA producer: one 128 x 64-byte box per tile (64-byte swizzle),
+//               rows past S filled with zeros;
+//   warp 1      MMA issuer: loads the tile's 128 scale words (two tiles ahead),
+//               writes them in the 32x16-byte scale-factor layout, tcgen05.cp to
+//               TMEM, and two tcgen05.mma kind::mxf4 (K = 64 each) into a
+//               128 x 256 fp32 accumulator;
+//   warps 2-9   epilogue: TMEM lane = key; each pair of warps on a lane quarter
+//               splits the G queries; w * max(0, .) summed over heads, masked
+//               to each query's window.
+// The CTA order is reversed so that the largest groups (the end of a causal
+// prefill) start first.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "paged_core.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kMqaThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kMqaStages = 4;
+constexpr int kN = 256;            // query-head columns per CTA
+constexpr int kEpiWarps = 8;
+
+struct MqaLayout {
+  static constexpr uint32_t kAccCol = 0;            // 256 fp32 columns
+  static constexpr uint32_t kSfbCol = kN;           // 8 columns (two 128-row atoms)
+  static constexpr uint32_t kSfaCol = kN + 8;       // 4 columns
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr size_t kA = 0;                                        // stages x 8192
+  static constexpr size_t kB = kA + (size_t)kMqaStages * kTileValBytes;  // 256 x 64
+  static constexpr size_t kSfa = kB + (size_t)kN * kValBytes;            // stages x 512
+  static constexpr size_t kSfb = kSfa + (size_t)kMqaStages * 512;        // 2 x 512
+  static constexpr size_t kW = kSfb + 1024;                              // 256 floats
+  static constexpr size_t kWin = kW + (size_t)kN * 4;                    // 2 x 8 int32
+  static constexpr size_t kBars = align_up(kWin + 64, 16);
+  static constexpr int kNumBars = 2 * kMqaStages + 2;
+  static constexpr size_t kMisc = kBars + (size_t)kNumBars * 8;
+  static constexpr size_t kEnd = align_up(kMisc + 16, 1024);
+};
+
+template <int H>
+__global__ void __launch_bounds__(kMqaThreads, 1)
+    mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_k, const MqaArgs p) {
+  constexpr int G = kN / H;       // queries per CTA
+  constexpr int GH = G / 2;       // queries per epilogue warp
+  using Lay = MqaLayout;
+  const int64_t n_groups = (p.T + G - 1) / G;
+  const int64_t g = n_groups - 1 - (int64_t)blockIdx.x;
+  const int64_t t0 = g * G;
+
+  uint8_t* sm = aligned_smem_base();
+  uint8_t* sA = sm + Lay::kA;
+  uint8_t* sB = sm + Lay::kB;
+  uint8_t* sSfa = sm + Lay::kSfa;
+  uint8_t* sSfb = sm + Lay::kSfb;
+  float* sW = reinterpret_cast<float*>(sm + Lay::kW);
+  int32_t* sStart = reinterpret_cast<int32_t*>(sm + Lay::kWin);
+  int32_t* sEnd = sStart + 8;
+  const uint32_t bars = smem_u32(sm + Lay::kBars);
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kMqaStages + s); };
+  const uint32_t tfull = bars + 8u * (2 * kMqaStages);
+  const uint32_t tempty = bars + 8u * (2 * kMqaStages + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::kMisc + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- windows of the group's queries (clamped to [0, S])
+  if (threadIdx.x < G) {
+    const int64_t t = t0 + threadIdx.x;
+    int32_t st = 0, en = 0;
+    if (t < p.T) {
+      const int32_t st0 = __ldg(p.row_start + t), en0 = __ldg(p.row_end + t);
+      st = st0 < 0 ? 0 : (st0 > p.S ? (int32_t)p.S : st0);
+      en = en0 < st ? st : (en0 > p.S ? (int32_t)p.S : en0);
+      if (st != st0 || en != en0) count_bad_input(p.errors);
+    }
+    sStart[threadIdx.x] = st;
+    sEnd[threadIdx.x] = en;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMqaStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kEpiWarps);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  {
+    // B operand: query heads (t0 + j, h) as rows n = j*H + h, 64-byte swizzle;
+    // rows of queries past T are zero.
+    const int64_t rows_avail = (p.T - t0) * H;
+    const uint8_t* qv = p.q_vals + t0 * H * kValBytes;
+    for (int i = threadIdx.x; i < kN * 4; i += kMqaThreads) {
+      const int n = i >> 2, ch = i & 3;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < rows_avail) v = __ldg(reinterpret_cast<const uint4*>(qv + n * kValBytes) + ch);
+      *reinterpret_cast<uint4*>(sB + n * kValBytes + ((ch ^ ((n >> 1) & 3)) << 4)) = v;
+    }
+    const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + t0 * H;
+    for (int n = threadIdx.x; n < kN; n += kMqaThreads) {
+      const uint32_t wv = n < rows_avail ? __ldg(qs + n) : 0u;
+      const int a = n >> 7, r = n & 127;
+      *reinterpret_cast<uint32_t*>(sSfb + a * 512 + 16 * (r % 32) + 4 * (r / 32)) = wv;
+      sW[n] = n < rows_avail ? __ldg(p.weights + t0 * H + n) : 0.f;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- key tiles covering the union of the windows
+  int32_t kmin = INT32_MAX, kmax = 0;
+  for (int j = 0; j < G; ++j) {
+    if (sEnd[j] > sStart[j]) {
+      kmin = min(kmin, sStart[j]);
+      kmax = max(kmax, sEnd[j]);
+    }
+  }
+  const int tile_lo = kmax > 0 ? kmin / kTileKeys : 0;
+  const int tile_hi = kmax > 0 ? (kmax + kTileKeys - 1) / kTileKeys : 0;
+  const int n_tiles = tile_hi - tile_lo;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tm_k);
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kMqaStages;
+        if (!mbar_wait(empty_bar(s), ((i / kMqaStages) & 1) ^ 1, abort)) {
+          flag_timeout(p.errors, kTimeoutProducer);
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), kTileValBytes);
+        tma_load_2d(smem_u32(sA + (size_t)s * kTileValBytes), &tm_k, 0,
+                    (tile_lo + i) * kTileKeys, full_bar(s));
+        ++issued;
+      }
+      for (int i = issued > kMqaStages ? issued - kMqaStages : 0; i < issued; ++i)
+        if (!mbar_wait_drain(full_bar(i % kMqaStages), (i / kMqaStages) & 1))
+          flag_timeout(p.errors, kTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint32_t sfb_t = tmem + Lay::kSfbCol;
+    const uint32_t sfa_t = tmem + Lay::kSfaCol;
+    if (lane == 0 && n_tiles > 0) {
+      tmem_cp_32x128b_x4(sfb_t, smem_desc(smem_u32(sSfb), 16, 128, kLayoutNone));
+      tmem_cp_32x128b_x4(sfb_t + 4, smem_desc(smem_u32(sSfb + 512), 16, 128, kLayoutNone));
+    }
+    __syncwarp();
+    const uint32_t* ksc = reinterpret_cast<const uint32_t*>(p.k_scales);
+    auto load_scales = [&](int i) {
+      uint4 r = make_uint4(0, 0, 0, 0);
+      if (i < n_tiles) {
+        const int64_t k0 = (int64_t)(tile_lo + i) * kTileKeys + lane;
+        r.x = k0 < p.S ? __ldg(ksc + k0) : 0u;
+        r.y = k0 + 32 < p.S ? __ldg(ksc + k0 + 32) : 0u;
+        r.z = k0 + 64 < p.S ? __ldg(ksc + k0 + 64) : 0u;
+        r.w = k0 + 96 < p.S ? __ldg(ksc + k0 + 96) : 0u;
+      }
+      return r;
+    };
+    uint4 sc_next = load_scales(0);
+    uint4 sc_next2 = load_scales(1);
+    const uint64_t b_desc = smem_desc(smem_u32(sB), 16, 512, kLayoutSw64);
+    int issued = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i % kMqaStages;
+      const uint4 sc = sc_next;
+      sc_next = sc_next2;
+      sc_next2 = load_scales(i + 2);
+      const bool ok = mbar_wait(full_bar(s), (i / kMqaStages) & 1, abort) &&
+                      mbar_wait(tempty, (i & 1) ^ 1, abort);
+      if (!ok) {
+        if (lane == 0) flag_timeout(p.errors, kTimeoutMma);
+        break;
+      }
+      tc_fence_after();
+      *reinterpret_cast<uint4*>(sSfa + (size_t)s * 512 + 16 * lane) = sc;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tmem_cp_32x128b_x4(sfa_t, smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
+        const uint64_t a_desc =
+            smem_desc(smem_u32(sA + (size_t)s * kTileValBytes), 16, 512, kLayoutSw64);
+        mma_mxf4(tmem + Lay::kAccCol, a_desc, b_desc, mxf4_idesc(kN, 0, 0), sfa_t, sfb_t, 0u);
+        mma_mxf4(tmem + Lay::kAccCol, a_desc + 2, b_desc + 2, mxf4_idesc(kN, 2, 2), sfa_t, sfb_t,
+                 1u);
+        mma_commit(empty_bar(s));
+        mma_commit(tfull);
+      }
+      __syncwarp();
+      ++issued;
+    }
+    if (lane == 0 && issued > 0 && !mbar_wait_drain(tfull, (issued - 1) & 1))
+      flag_timeout(p.errors, kTimeoutDrain);
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int e = warp - 2;
+    const int quarter = warp & 3;
+    const int half = e / 4;                 // which half of the group's queries
+    const int m = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    int32_t st[GH], en[GH];
+#pragma unroll
+    for (int j = 0; j < GH; ++j) {
+      st[j] = sStart[half * GH + j];
+      en[j] = sEnd[half * GH + j];
+    }
+    for (int i = 0; i < n_tiles; ++i) {
+      if (!mbar_wait(tfull, i & 1, abort)) {
+        if (lane == 0) flag_timeout(p.errors, kTimeoutEpilogue);
+        break;
+      }
+      tc_fence_after();
+      float d[GH * H];
+#pragma unroll
+      for (int part = 0; part < GH * H / 32; ++part)
+        tmem_ld32_sync(lane_addr + Lay::kAccCol + (uint32_t)(half * GH * H + 32 * part),
+                       *reinterpret_cast<float(*)[32]>(&d[32 * part]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      const int64_t key = (int64_t)(tile_lo + i) * kTileKeys + m;
+      float logit[GH];
+      weighted_relu_sum<H, GH>(sW + half * GH * H, d, logit);
+#pragma unroll
+      for (int j = 0; j < GH; ++j) {
+        const int64_t t = t0 + half * GH + j;
+        if (t >= p.T) break;
+        float* row = p.logits + t * p.ld;
+        if (key >= st[j] && key < en[j])
+          row[key] = logit[j];
+        else if (p.clean && key < p.S)
+          row[key] = -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+  if (p.clean) {
+    // -inf for the columns of [0, S) that no tile covers
+    const int64_t lo_end = (int64_t)tile_lo * kTileKeys;
+    const int64_t hi_begin = (int64_t)tile_hi * kTileKeys;
+    for (int j = 0; j < G; ++j) {
+      const int64_t t = t0 + j;
+      if (t >= p.T) break;
+      float* row = p.logits + t * p.ld;
+      const int64_t lo1 = n_tiles > 0 ? lo_end : p.S;
+      for (int64_t s = threadIdx.x; s < lo1 && s < p.S; s += kMqaThreads) row[s] = -INFINITY;
+      if (n_tiles > 0)
+        for (int64_t s = hi_begin + threadIdx.x; s < p.S; s += kMqaThreads) row[s] = -INFINITY;
+    }
+  }
+}
+
+template <int H>
+cudaError_t launch_h(const CUtensorMap& tm, const MqaArgs& a, cudaStream_t stream) {
+  const size_t smem = MqaLayout::kEnd + 1024;
+  auto kern = mqa_logits_kernel<H>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  constexpr int G = kN / H;
+  const int64_t groups = (a.T + G - 1) / G;
+  kern<<<(unsigned)groups, kMqaThreads, smem, stream>>>(tm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs& a,
+                              cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  if (H == 32) return launch_h<32>(tm_kvals, a, stream);
+  if (H == 64) return launch_h<64>(tm_kvals, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace idx

@@ -14,6 +14,7 @@
 #include "idx.h"
 #include "common.cuh"
 #include "launch.h"
+#include "paged_core.cuh"
 
 namespace {
 
@@ -141,6 +142,17 @@ idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, in
   return IDX_OK;
 }
 
+// Split each sequence's columns [0, cols) into chunks of whole 128-key tiles:
+// about four CTAs per SM over the whole batch, 2..64 tiles per CTA.
+void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms) {
+  const int64_t tiles = (cols + 127) / 128;
+  int64_t per = (tiles * a.B + 4LL * sms - 1) / (4LL * sms);
+  per = per < 2 ? 2 : (per > idx::kMaxTilesPerCta ? idx::kMaxTilesPerCta : per);
+  a.tiles_per_cta = (int32_t)per;
+  const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
+  a.chunks = chunks > INT32_MAX ? -1 : (int32_t)chunks;
+}
+
 }  // namespace
 
 extern "C" {
@@ -242,15 +254,8 @@ idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, 
   a.clean = clean ? 1 : 0;
   a.errors = errors;
   const int64_t cap = (int64_t)max_blocks * 64;
-  const int64_t cols = a.clean ? ld : (ld < cap ? ld : cap);
-  const int64_t tiles = (cols + 127) / 128;
-  // about four CTAs per SM over the whole batch, 2..64 tiles each
-  int64_t per = (tiles * B + 4LL * sms - 1) / (4LL * sms);
-  per = per < 2 ? 2 : (per > 64 ? 64 : per);
-  a.tiles_per_cta = (int32_t)per;
-  const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
-  if (chunks > INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "ld too large");
-  a.chunks = (int32_t)chunks;
+  set_paged_chunking(a, a.clean ? ld : (ld < cap ? ld : cap), sms);
+  if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "ld too large");
   return from_cuda(idx::launch_paged_logits(tv, ts, H, next_n, a, (cudaStream_t)stream),
                    "paged_mqa_logits launch");
 }
@@ -335,8 +340,11 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   if (s != IDX_OK) return s;
   if (B == 0) return ok();
   if (!out_idx) return fail(IDX_ERR_INVALID_ARG, "null out_idx");
-  int32_t per = 0, chunks = 0;
-  const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, &per, &chunks);
+  if ((int64_t)B * next_n > 65535)
+    return fail(IDX_ERR_INVALID_ARG, "B*next_n=%d above 65535", B * next_n);
+  int sms = 0;
+  if ((s = current_device_ok(&sms)) != IDX_OK) return s;
+  const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, nullptr, nullptr);
   if (workspace_bytes < need || workspace == nullptr)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
   if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
@@ -355,8 +363,7 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   a.B = B;
   a.max_blocks = max_blocks;
   a.clean = 0;
-  a.tiles_per_cta = per;
-  a.chunks = chunks;
+  set_paged_chunking(a, (int64_t)max_blocks * 64, sms);
   a.topk = k;
   a.out_idx = out_idx;
   a.workspace = workspace;

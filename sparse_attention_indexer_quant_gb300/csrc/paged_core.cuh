@@ -9,7 +9,8 @@
 namespace idx {
 
 constexpr int kPagedThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kStages = 4;
+constexpr int kStages = 6;
+constexpr int kMaxTilesPerCta = 64;
 constexpr int kTileKeys = 128;       // MMA M: two pages
 constexpr int kTileValBytes = kTileKeys * kValBytes;  // 8192
 
@@ -21,7 +22,9 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 // Shared-memory and tensor-memory plan for N = NH query-head columns.
 template <int NH>
 struct PagedLayout {
-  static constexpr int kAccBufs = NH <= 64 ? 2 : 1;
+  // accumulator buffers: as many as keep a CTA within 128 TMEM columns (N = 32,
+  // 64) or 256 columns (N = 128), so that 2-4 CTAs share an SM
+  static constexpr int kAccBufs = NH == 32 ? 3 : 1;
   static constexpr uint32_t kSfbCol = kAccBufs * NH;     // 4 columns
   static constexpr uint32_t kSfaCol = kSfbCol + 4;       // 4 columns per accumulator
   static constexpr uint32_t kTmemCols = tmem_cols_for(kSfaCol + 4 * kAccBufs);
@@ -31,7 +34,8 @@ struct PagedLayout {
   static constexpr size_t kSfa = kSfRaw + (size_t)kStages * 512;     // stages x 512
   static constexpr size_t kSfb = kSfa + (size_t)kStages * 512;       // 512
   static constexpr size_t kW = kSfb + 512;                           // NH floats
-  static constexpr size_t kBars = align_up(kW + (size_t)NH * 4, 16);
+  static constexpr size_t kBt = kW + (size_t)NH * 4;                 // 2 x 64 page ids
+  static constexpr size_t kBars = align_up(kBt + 2 * kMaxTilesPerCta * 4, 16);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs;
   static constexpr size_t kMisc = kBars + (size_t)kNumBars * 8;      // tmem base, abort
   static constexpr size_t kExtra = align_up(kMisc + 16, 1024);       // epilogue's region
@@ -128,6 +132,7 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::kMisc + 4);
   uint8_t* extra = sm + Lay::kExtra;
+  int32_t* sBt = reinterpret_cast<int32_t*>(sm + Lay::kBt);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -168,6 +173,12 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
     }
     for (int n = threadIdx.x; n < NH; n += kPagedThreads)
       sW[n] = __ldg(p.weights + (int64_t)c.b * NH + n);
+    // the chunk's page ids; pages past the context are not read
+    const int32_t* bt = p.block_table + (int64_t)c.b * p.max_blocks + c.k0 / kPage;
+    const int n_pages = (int)((c.L - c.k0 + kPage - 1) / kPage);
+    for (int i = threadIdx.x; i < 2 * c.n_tiles; i += kPagedThreads)
+      sBt[i] = i < n_pages ? __ldg(bt + i) : 0;
+    Ep::init(extra);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -180,8 +191,6 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
     if (lane == 0) {
       tma_prefetch_desc(tm_vals);
       tma_prefetch_desc(tm_scales);
-      const int32_t* bt = p.block_table + (int64_t)c.b * p.max_blocks;
-      const int page0 = (int)(c.k0 / kPage);
       int issued = 0;
       for (int i = 0; i < c.n_tiles; ++i) {
         const int s = i % kStages;
@@ -189,10 +198,9 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
           flag_timeout(p.errors, kTimeoutProducer);
           break;
         }
-        const int pg = page0 + 2 * i;
-        const bool two = (int64_t)(pg + 1) * kPage < c.L;
-        int32_t id0 = __ldg(bt + pg);
-        int32_t id1 = two ? __ldg(bt + pg + 1) : 0;
+        const bool two = c.k0 + (int64_t)(2 * i + 1) * kPage < c.L;
+        const int32_t id0 = sBt[2 * i];
+        const int32_t id1 = sBt[2 * i + 1];
         // out-of-range ids load the TMA fill (zeros) instead of faulting
         if (id0 < 0 || id0 >= p.num_blocks) count_bad_input(p.errors);
         if (two && (id1 < 0 || id1 >= p.num_blocks)) count_bad_input(p.errors);

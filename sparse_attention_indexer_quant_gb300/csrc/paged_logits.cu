@@ -30,6 +30,7 @@ template <int H, int NEXT_N>
 struct UnfusedEpilogue {
   static constexpr int NH = H * NEXT_N;
   static constexpr size_t kExtraSmem = 0;
+  __device__ __forceinline__ static void init(uint8_t*) {}
 
   // Called once per tile by every epilogue thread with its key's NH dot
   // products (column n = j*H + h).

@@ -2,10 +2,11 @@
 // top_k_per_row into topk_indices_buffer; the rows shorter than k are padded
 // with -1).
 //
-// One CTA per row.  The first digit's histogram is taken straight from the row
-// in global memory; the elements in the threshold bin are then compacted into
-// shared memory (when they fit) while the elements above it are emitted, and
-// the remaining digits run on the compacted set.
+// One CTA per row.  Pass 1 builds the coarse histogram of the row straight
+// from global memory; pass 2 emits the elements above the boundary bin and
+// compacts the boundary bin's elements into shared memory (when they fit),
+// where the exact threshold is found; otherwise the exact passes read the row
+// again, restricted to the boundary bin.
 #include "common.cuh"
 #include "launch.h"
 #include "topk_select.cuh"
@@ -14,7 +15,7 @@ namespace idx {
 namespace {
 
 constexpr int kTopkThreads = 512;
-constexpr int kCandCap = 4096;
+constexpr int kCandCap = 3584;
 
 struct GlobalRow {
   const float* x;
@@ -26,7 +27,7 @@ struct GlobalRow {
 };
 
 struct TopkSmem {
-  SelectScratch sc;
+  SelectScratch sel;
   uint32_t cand_keys[kCandCap];
   int32_t cand_idx[kCandCap];
   uint32_t n_cand;
@@ -48,35 +49,38 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
     return;
   }
   const GlobalRow src{logits + row * ld + st, len};
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sm.sel.hist[i] = 0;
   if (threadIdx.x == 0) {
-    sm.sc.out_count = 0;
+    sm.sel.s.count = 0;
     sm.n_cand = 0;
   }
-  auto emit = [&](uint32_t, int32_t idx) { orow[atomicAdd(&sm.sc.out_count, 1u)] = idx; };
-
-  digit_histogram(sm.sc, src, 0, 0u, 0u);
-  find_threshold_bin(sm.sc, kRadixBins, (uint32_t)k);
-  const uint32_t b1 = sm.sc.bin;
-  const uint32_t need = (uint32_t)k - sm.sc.above;
-  const bool fits = sm.sc.hist[b1] <= (uint32_t)kCandCap;
   __syncthreads();
-  src.for_each([&](uint32_t key, int32_t idx) {
-    const uint32_t dg = key >> 21;
-    if (dg > b1) {
-      emit(key, idx);
-    } else if (dg == b1 && fits) {
-      const uint32_t slot = atomicAdd(&sm.n_cand, 1u);
-      sm.cand_keys[slot] = key;
-      sm.cand_idx[slot] = idx;
+  src.for_each([&](uint32_t key, int32_t) { hist_add(sm.sel.hist, coarse_bin(key), true); });
+  __syncthreads();
+  find_threshold_bin(sm.sel.hist, kCoarseBins, (uint32_t)k, sm.sel.s);
+  const uint32_t b1 = sm.sel.s.bin;
+  const uint32_t above = sm.sel.s.above;
+  const bool fits = sm.sel.hist[b1] <= (uint32_t)kCandCap;
+  __syncthreads();
+  src.for_each([&](uint32_t key, int32_t i) {
+    const uint32_t bin = coarse_bin(key);
+    const uint32_t slot = warp_claim(&sm.sel.s.count, bin > b1);
+    if (bin > b1) orow[slot] = i;
+    if (bin == b1 && fits) {
+      const uint32_t c = atomicAdd(&sm.n_cand, 1u);
+      sm.cand_keys[c] = key;
+      sm.cand_idx[c] = i;
     }
   });
   __syncthreads();
-  const uint32_t prefix = b1 << 21, mask = 0x7FFu << 21;
+  auto emit = [&](uint32_t, int32_t i) { orow[warp_claim(&sm.sel.s.count, true)] = i; };
+  const uint32_t need = (uint32_t)k - above;
   if (fits) {
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)sm.n_cand};
-    radix_select(sm.sc, cand, need, 1, prefix, mask, emit);
+    radix_select(sm.sel.hist, sm.sel.s, cand, need, 0u, 0u, emit);
   } else {
-    radix_select(sm.sc, src, need, 1, prefix, mask, emit);
+    radix_select(sm.sel.hist, sm.sel.s, src, need, b1 << kCoarseShift,
+                 0xFFFFFFFFu << kCoarseShift, emit);
   }
 }
 

@@ -1,40 +1,74 @@
-// Block-wide radix selection of the k largest fp32 values (vLLM API docs
+// Block-wide selection of the k largest fp32 values (vLLM API docs
 // "vllm.models.glm5next.nvidia.sparse_indexer": top_k_per_row).
 //
-// Values are mapped to order-preserving uint32 keys and the threshold key is
-// found digit by digit (11, 11 and 10 bits, most significant first) from
-// shared-memory histograms.  At every digit the elements whose digit is above
-// the threshold digit are certainly selected and are emitted at once; the
-// rest of the search continues among the elements that share the threshold
-// prefix.  Elements equal to the final threshold key fill the remaining slots
-// in arrival order, so equal values may be taken in any order.
+// Values are mapped to order-preserving uint32 keys.  A coarse histogram over
+// the top 12 key bits (sign, exponent and 3 mantissa bits: 8 bins per octave
+// at any magnitude) locates the bin holding the k-th largest value; everything
+// in higher bins is selected outright, and the exact threshold inside the
+// boundary bin is found by radix passes on the full key (11, 11 and 10 bits)
+// over the boundary elements only.  Elements equal to the final threshold key
+// fill the remaining slots in arrival order, so equal values may be taken in
+// any order.
+//
+// Histogram updates are aggregated per warp (one shared-memory atomic per
+// distinct bin in a warp), which keeps clustered values from serialising.
 //
 // A source visits (key, index) pairs: `src.for_each(f)` calls f(key, idx) for
 // this thread's share of the elements.  Every thread of the block must call
 // the routines below together.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace idx {
 
+constexpr int kCoarseShift = 20;
+constexpr int kCoarseBins = 1 << (32 - kCoarseShift);   // 4096
 constexpr int kRadixBins = 2048;
 
-struct SelectScratch {
-  uint32_t hist[kRadixBins];
+__device__ __forceinline__ uint32_t coarse_bin(uint32_t key) { return key >> kCoarseShift; }
+
+struct ScanScratch {
   uint32_t warp_sums[32];
   uint32_t bin;
   uint32_t above;
-  uint32_t out_count;
+  uint32_t count;
   uint32_t tie_count;
-  uint32_t aux;
 };
 
-__device__ __forceinline__ constexpr int digit_shift(int d) { return d == 0 ? 21 : d == 1 ? 10 : 0; }
-__device__ __forceinline__ constexpr uint32_t digit_mask(int d) { return d == 2 ? 0x3FFu : 0x7FFu; }
+struct SelectScratch {
+  uint32_t hist[kCoarseBins];
+  ScanScratch s;
+};
+
+// atomicAdd(&hist[bin], 1) for every lane with pred, one atomic per distinct
+// bin in the warp.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool pred) {
+  const uint32_t active = __activemask();
+  const uint32_t want = __ballot_sync(active, pred);
+  if (!pred) return;
+  const uint32_t peers = __match_any_sync(want, bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// Returns a distinct slot from *counter for every lane with pred (one atomic
+// per warp), or 0xFFFFFFFF for lanes without.
+__device__ __forceinline__ uint32_t warp_claim(uint32_t* counter, bool pred) {
+  const uint32_t active = __activemask();
+  const uint32_t want = __ballot_sync(active, pred);
+  if (!pred) return 0xFFFFFFFFu;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(want) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(want));
+  base = __shfl_sync(want, base, leader);
+  return base + __popc(want & ((1u << lane) - 1u));
+}
 
 // Exclusive prefix sum of v over the threads of the block, in thread order.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectScratch& sc) {
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanScratch& sc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
   uint32_t x = v;
@@ -52,7 +86,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectScrat
       const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, t, o);
       if (lane >= o) t += y;
     }
-    if (lane < nwarps) sc.warp_sums[lane] = t;  // inclusive totals
+    if (lane < nwarps) sc.warp_sums[lane] = t;
   }
   __syncthreads();
   const uint32_t before = warp == 0 ? 0u : sc.warp_sums[warp - 1];
@@ -64,15 +98,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectScrat
 // Finds the bin b of hist[0, nbins) with count(bins > b) < need <= count(bins >= b)
 // and stores b and count(bins > b) in sc.bin / sc.above.  Requires
 // 1 <= need <= total count.
-__device__ __forceinline__ void find_threshold_bin(SelectScratch& sc, int nbins, uint32_t need) {
+__device__ __forceinline__ void find_threshold_bin(const uint32_t* hist, int nbins, uint32_t need,
+                                                   ScanScratch& sc) {
   const int nt = blockDim.x;
   const int per = (nbins + nt - 1) / nt;
-  // thread t owns bins (hi - per, hi] counted from the top
-  const int hi = nbins - 1 - threadIdx.x * per;
+  const int hi = nbins - 1 - (int)threadIdx.x * per;   // this thread's bins: (hi - per, hi]
   uint32_t local = 0;
   for (int q = 0; q < per; ++q) {
     const int bin = hi - q;
-    if (bin >= 0) local += sc.hist[bin];
+    if (bin >= 0) local += hist[bin];
   }
   const uint32_t excl = block_exclusive_scan(local, sc);
   if (excl < need && need <= excl + local) {
@@ -80,7 +114,7 @@ __device__ __forceinline__ void find_threshold_bin(SelectScratch& sc, int nbins,
     for (int q = 0; q < per; ++q) {
       const int bin = hi - q;
       if (bin < 0) break;
-      const uint32_t h = sc.hist[bin];
+      const uint32_t h = hist[bin];
       if (run + h >= need) {
         sc.bin = (uint32_t)bin;
         sc.above = run;
@@ -92,33 +126,29 @@ __device__ __forceinline__ void find_threshold_bin(SelectScratch& sc, int nbins,
   __syncthreads();
 }
 
-// Histogram of digit d over the elements matching (key & mask) == prefix.
-template <class Src>
-__device__ __forceinline__ void digit_histogram(SelectScratch& sc, const Src& src, int d,
-                                                uint32_t prefix, uint32_t mask) {
-  const int nb = (int)digit_mask(d) + 1;
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) sc.hist[i] = 0;
-  __syncthreads();
-  const int sh = digit_shift(d);
-  const uint32_t dm = digit_mask(d);
-  src.for_each([&](uint32_t key, int32_t) {
-    if ((key & mask) == prefix) atomicAdd(&sc.hist[(key >> sh) & dm], 1u);
-  });
-  __syncthreads();
-}
+__device__ __forceinline__ constexpr int digit_shift(int d) { return d == 0 ? 21 : d == 1 ? 10 : 0; }
+__device__ __forceinline__ constexpr uint32_t digit_mask(int d) { return d == 2 ? 0x3FFu : 0x7FFu; }
 
 // Emits (through emit(key, idx)) exactly `need` elements: the `need` largest
-// keys among those matching (key & mask) == prefix, searching from digit d0.
+// keys among those of src matching (key & mask) == prefix.  hist must hold at
+// least kRadixBins words of scratch.
 template <class Src, class Emit>
-__device__ __forceinline__ void radix_select(SelectScratch& sc, const Src& src, uint32_t need,
-                                             int d0, uint32_t prefix, uint32_t mask,
+__device__ __forceinline__ void radix_select(uint32_t* hist, ScanScratch& sc, const Src& src,
+                                             uint32_t need, uint32_t prefix, uint32_t mask,
                                              Emit emit) {
-  for (int d = d0; d < 3 && need > 0; ++d) {
-    digit_histogram(sc, src, d, prefix, mask);
-    find_threshold_bin(sc, (int)digit_mask(d) + 1, need);
-    const uint32_t b = sc.bin, above = sc.above;
+  for (int d = 0; d < 3 && need > 0; ++d) {
     const int sh = digit_shift(d);
     const uint32_t dm = digit_mask(d);
+    const int nb = (int)dm + 1;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    src.for_each([&](uint32_t key, int32_t) {
+      const bool m = (key & mask) == prefix;
+      hist_add(hist, (key >> sh) & dm, m);
+    });
+    __syncthreads();
+    find_threshold_bin(hist, nb, need, sc);
+    const uint32_t b = sc.bin, above = sc.above;
     if (above > 0) {
       src.for_each([&](uint32_t key, int32_t idx) {
         if ((key & mask) == prefix && ((key >> sh) & dm) > b) emit(key, idx);
@@ -149,6 +179,17 @@ struct SmemPairs {
   template <class F>
   __device__ __forceinline__ void for_each(F f) const {
     for (int i = threadIdx.x; i < n; i += blockDim.x) f(keys[i], idx[i]);
+  }
+};
+
+// Elements of a global-memory array of keys with their indices (read through L2).
+struct GlobalPairs {
+  const uint32_t* keys;
+  const int32_t* idx;
+  int64_t n;
+  template <class F>
+  __device__ __forceinline__ void for_each(F f) const {
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) f(__ldcg(keys + i), __ldcg(idx + i));
   }
 };
 

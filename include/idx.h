@@ -200,6 +200,30 @@ IDX_API idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q
                                  idx_device_errors* errors, idx_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * idx_paged_logits_topk_noalloc -- idx_paged_logits_topk for callers that
+ * cannot allocate device memory: an engine whose allocator is frozen after
+ * start-up, a plugin host that passes raw buffers but offers no allocator, or a
+ * latency-critical step that must not pay for cudaMalloc (it can block on the
+ * device).  The pages have no counterpart for this entry; it only changes where
+ * the scratch comes from.
+ *   Arguments as for idx_paged_logits_topk, without workspace/workspace_bytes.
+ *   The scratch is a 32 MiB array inside the library: every GPU that loads the
+ *   library reserves it until the process exits.  Its device address is looked
+ *   up on the first call on each device (with that device current), so make
+ *   that first call before any stream capture.
+ *   A batch whose idx_paged_logits_topk_workspace_bytes exceeds 32 MiB is
+ *   rejected with IDX_ERR_INVALID_ARG (and a message on stderr); use
+ *   idx_paged_logits_topk with a caller workspace for it.
+ *   All calls share the one scratch array: calls that overlap on the GPU race.
+ *   Every call clears the parts that must start at zero.
+ * ------------------------------------------------------------------------ */
+IDX_API idx_status idx_paged_logits_topk_noalloc(
+    const uint8_t* q_vals, const uint8_t* q_scales, int32_t B, int32_t next_n, int32_t H,
+    const uint8_t* kcache, int64_t num_blocks, int32_t page_size, const int32_t* block_table,
+    int32_t max_blocks, const int32_t* context_lens, const float* weights, int32_t k,
+    int32_t* out_idx, idx_device_errors* errors, idx_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * idx_gather_k -- copy sequences' cached tokens into contiguous value/scale
  * arrays (PR #48558 "Live validation": the shared cp_gather reader).
  *   seq_lens     [B] int32 tokens to copy per sequence (<= max_blocks*page_size).

@@ -43,6 +43,8 @@ SIGNATURES = {
                                              _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "idx_gather_k": (ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _I32, _P, _P, _I64, _P,
                                     _P]),
+    "idx_paged_logits_topk_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _I32, _P,
+                                                     _I32, _P, _P, _I32, _P, _P, _P]),
 }
 
 
@@ -199,6 +201,23 @@ def paged_logits_topk(q_vals, q_scales, weights, kcache, block_table, context_le
         _ptr(q_vals), _ptr(q_scales), B, next_n, H, _ptr(kcache), kcache.shape[0], PAGE_SIZE,
         _ptr(block_table), max_blocks, _ptr(context_lens), _ptr(weights), k, _ptr(idx),
         _ptr(workspace), workspace.numel(), _ptr(errors), _stream(stream)))
+    return idx
+
+
+def paged_logits_topk_noalloc(q_vals, q_scales, weights, kcache, block_table, context_lens,
+                              next_n: int, H: int, k: int = 2048, out=None, errors=None,
+                              stream=None):
+    """idx_paged_logits_topk_noalloc: the fused decode path with the library's
+    built-in 32 MiB scratch instead of a caller workspace (for callers that
+    cannot allocate device memory)."""
+    B, max_blocks = _paged_common(q_vals, q_scales, weights, kcache, block_table, context_lens,
+                                  next_n, H)
+    idx = out if out is not None else torch.empty((B * next_n, k), dtype=torch.int32,
+                                                  device=q_vals.device)
+    _check("idx_paged_logits_topk_noalloc", lib.idx_paged_logits_topk_noalloc(
+        _ptr(q_vals), _ptr(q_scales), B, next_n, H, _ptr(kcache), kcache.shape[0], PAGE_SIZE,
+        _ptr(block_table), max_blocks, _ptr(context_lens), _ptr(weights), k, _ptr(idx),
+        _ptr(errors), _stream(stream)))
     return idx
 
 

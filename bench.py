@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--ref-budget-s", type=float, default=90.0,
+                    help="reference arm: seconds of oracle work for warmup + steps")
     ap.add_argument("--workload", default="batched_decode",
                     choices=sorted(WORKLOADS),
                     help="decode workload; the default is the headline configuration")
@@ -376,7 +378,7 @@ def run_reference(args, rank, world):
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     p = make_workload(args.workload)
     # calibrate the per-step sample so that warmup + steps take about 90 s
-    budget_s = 90.0
+    budget_s = args.ref_budget_s
     n_steps = args.steps + args.warmup
     probe = cpu_baseline(p, 1)
     rate = probe["value"]
@@ -431,13 +433,16 @@ def run_reference(args, rank, world):
 _PG = None
 
 
-def init_dist(world):
+def init_dist(world, backend=None):
+    """One process per GPU (torchrun); the process group carries only the
+    barrier and the max-over-ranks of the timing, never the data path."""
     global _PG
     if world <= 1:
         return
     import torch.distributed as dist
     if not dist.is_initialized():
-        backend = "nccl" if __import__("torch").cuda.is_available() else "gloo"
+        if backend is None:
+            backend = "nccl" if __import__("torch").cuda.is_available() else "gloo"
         dist.init_process_group(backend)
     _PG = dist
 

@@ -119,16 +119,7 @@ struct SelectSmem {
   int32_t cand_idx[kSelCap];
   uint32_t ticket;
   uint32_t slot;
-};
-
-struct WsRowSegment {
-  const float* x;
-  int64_t lo, hi;
-  template <class F>
-  __device__ __forceinline__ void for_each(F f) const {
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
-      f(float_key(__ldcg(x + i)), (int32_t)i);
-  }
+  uint32_t slot_fill;
 };
 
 __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedArgs p,
@@ -158,7 +149,7 @@ __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedAr
   }
   uint32_t* ghist = ws.hist + r * kCoarseBins;
   uint32_t* ctr = ws.ctr + r * 4;
-  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sm.sel.hist[i] = __ldcg(ghist + i);
+  copy_words_cg(sm.sel.hist, ghist, kCoarseBins);
   __syncthreads();
   find_threshold_bin(sm.sel.hist, kCoarseBins, k, sm.sel.s);
   const uint32_t b1 = sm.sel.s.bin;
@@ -167,7 +158,7 @@ __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedAr
   const float* x = ws.logits + r * ws.ldw;
   uint32_t* bkeys = ws.bkeys + r * ws.ldw;
   int32_t* bpos = ws.bpos + r * ws.ldw;
-  const WsRowSegment seg{x, lo, hi};
+  const GlobalLogits<true> seg{x, lo, hi};
   seg.for_each([&](uint32_t key, int32_t i) {
     const uint32_t bin = coarse_bin(key);
     const uint32_t slot = warp_claim(ctr + 0, bin > b1);
@@ -185,15 +176,20 @@ __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedAr
   if (sm.ticket != gridDim.x - 1) return;
   __threadfence();
   // last CTA of the row: the exact remainder from the boundary bin
-  if (threadIdx.x == 0) sm.slot = above;
+  if (threadIdx.x == 0) {
+    sm.slot = above;
+    sm.slot_fill = 0;
+  }
+  __syncthreads();
   const uint32_t need = k - above;
   auto emit = [&](uint32_t, int32_t i) { orow[warp_claim(&sm.slot, true)] = i; };
   const GlobalPairs bset{bkeys, bpos, (int64_t)nb1};
   if (nb1 <= (uint32_t)kSelCap) {
-    for (uint32_t i = threadIdx.x; i < nb1; i += blockDim.x) {
-      sm.cand_keys[i] = __ldcg(bkeys + i);
-      sm.cand_idx[i] = __ldcg(bpos + i);
-    }
+    bset.for_each([&](uint32_t key, int32_t i) {
+      const uint32_t c = atomicAdd(&sm.slot_fill, 1u);
+      sm.cand_keys[c] = key;
+      sm.cand_idx[c] = i;
+    });
     __syncthreads();
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
     radix_select(sm.sel.hist, sm.sel.s, cand, need, 0u, 0u, emit);

@@ -17,15 +17,6 @@ namespace {
 constexpr int kTopkThreads = 512;
 constexpr int kCandCap = 3584;
 
-struct GlobalRow {
-  const float* x;
-  int64_t n;
-  template <class F>
-  __device__ __forceinline__ void for_each(F f) const {
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) f(float_key(__ldg(x + i)), (int32_t)i);
-  }
-};
-
 struct TopkSmem {
   SelectScratch sel;
   uint32_t cand_keys[kCandCap];
@@ -48,7 +39,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
     for (int i = threadIdx.x; i < k; i += blockDim.x) orow[i] = i < len ? i : -1;
     return;
   }
-  const GlobalRow src{logits + row * ld + st, len};
+  // positions are reported relative to the window start
+  const GlobalLogits<false> src{logits + row * ld + st, 0, len};
   for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sm.sel.hist[i] = 0;
   if (threadIdx.x == 0) {
     sm.sel.s.count = 0;

@@ -182,6 +182,12 @@ struct SmemPairs {
   }
 };
 
+// Global-memory sources load a batch of kBatch elements per thread into
+// registers before handing any of them to f, so that every thread keeps
+// kBatch independent loads in flight (f's atomics and stores would otherwise
+// keep the next load from issuing before the previous element is done).
+constexpr int kBatch = 8;
+
 // Elements of a global-memory array of keys with their indices (read through L2).
 struct GlobalPairs {
   const uint32_t* keys;
@@ -189,8 +195,68 @@ struct GlobalPairs {
   int64_t n;
   template <class F>
   __device__ __forceinline__ void for_each(F f) const {
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) f(__ldcg(keys + i), __ldcg(idx + i));
+    for (int64_t base = 0; base < n; base += (int64_t)kBatch * blockDim.x) {
+      uint32_t kk[kBatch];
+      int32_t ii[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = base + (int64_t)u * blockDim.x + threadIdx.x;
+        kk[u] = i < n ? __ldcg(keys + i) : 0u;
+        ii[u] = i < n ? __ldcg(idx + i) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = base + (int64_t)u * blockDim.x + threadIdx.x;
+        if (i < n) f(kk[u], ii[u]);
+      }
+    }
   }
 };
+
+// fp32 logits x[lo, hi) as keys with their positions; loads through L2 (ld.cg)
+// or the read-only path.
+template <bool kCg>
+struct GlobalLogits {
+  const float* x;
+  int64_t lo, hi;
+  template <class F>
+  __device__ __forceinline__ void for_each(F f) const {
+    const int64_t n = hi - lo;
+    for (int64_t base = 0; base < n; base += (int64_t)kBatch * blockDim.x) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = base + (int64_t)u * blockDim.x + threadIdx.x;
+        v[u] = i < n ? (kCg ? __ldcg(x + lo + i) : __ldg(x + lo + i)) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = base + (int64_t)u * blockDim.x + threadIdx.x;
+        if (i < n) f(float_key(v[u]), (int32_t)(lo + i));
+      }
+    }
+  }
+};
+
+// dst[0, n) = src[0, n) (n a multiple of 4, both 16-byte aligned), all loads
+// of a thread issued before its stores.
+__device__ __forceinline__ void copy_words_cg(uint32_t* dst, const uint32_t* src, int n) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const int n4 = n / 4;
+  for (int base = 0; base < n4; base += 4 * blockDim.x) {
+    uint4 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < n4) t[u] = __ldcg(s4 + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < n4) d4[i] = t[u];
+    }
+  }
+}
 
 }  // namespace idx

@@ -11,7 +11,7 @@ The cache holds the rest of every context before timing starts.
 
 The metric is key-tokens scored per second (sum over query rows of the keys
 in the row's window, per second of step time) with the algorithmic HBM GB/s
-beside it.  L2 is flushed (a 256 MiB memset) before every timed step and each
+beside it.  L2 is flushed (a 256 MiB buffer written, then read) before every timed step and each
 step is timed alone with CUDA events on the launching stream.
 
 --impl reference times the CPU oracle (the plain fp64 statement of the same
@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode K-tokens scored/s + HBM GB/s (paged MXFP4 MQA logits + top-k)"
 UNIT = "key-tokens/s"
 TOPK = 2048
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 256 << 20   # 2x the 129 MB L2
 FUSED_SOURCES = ["paged_topk.cu", "paged_core.cuh", "topk_select.cuh", "common.cuh"]
 
 
@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the secondary insert / prefill measurements")
     ap.add_argument("--ref-budget-s", type=float, default=90.0,
                     help="reference arm: seconds of oracle work for warmup + steps")
     ap.add_argument("--workload", default="batched_decode",
@@ -85,7 +87,8 @@ def workload_config(p, name="batched_decode"):
             "H": p.H, "head_dim": 128,
             "page_size": 64, "next_n": p.next_n, "topk": p.topk,
             "scored_key_tokens_per_step": int(scored_tokens(p)),
-            "l2": "flushed before every timed step (256 MiB memset)"}
+            "l2": "flushed before every timed step: a 256 MiB buffer (2x L2) written, then "
+                  "read back, so no input is resident and no dirty line is left"}
 
 
 def scored_tokens(p) -> int:
@@ -230,7 +233,16 @@ def run_ours(args, rank, world, local_rank):
     qv = torch.empty((p.rows * p.H, 64), dtype=torch.uint8, device=dev)
     qs = torch.empty((p.rows * p.H, 4), dtype=torch.uint8, device=dev)
     out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        # write a buffer twice the size of L2, then read it back: afterwards no
+        # input of the step is resident and no dirty line is left for the
+        # timed kernels to write back
+        flush.fill_(1)
+        torch.sum(flush, dtype=torch.int64, out=flush_sink)
+
     stream = torch.cuda.current_stream()
 
     def step():
@@ -242,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
                               out=out)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
         fused()
     torch.cuda.synchronize()
@@ -253,7 +265,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -294,7 +306,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(args.e2e_steps):
-        flush.zero_()
+        flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
@@ -304,6 +316,10 @@ def run_ours(args, rank, world, local_rank):
     e2e_mean = reduce_max(sum(e2e_ms) / len(e2e_ms), world, dev)
     # correctness spot check of the last e2e result against the device result
     assert torch.equal(h_out, out.cpu())
+
+    also = None
+    if rank == 0 and not args.no_also:
+        also = secondary_measurements(idx, dev, flush_l2, stream)
 
     cpu = None
     if rank == 0:
@@ -338,8 +354,80 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": e2e_mean},
         "gpu_launches": 3 * K,
         "clocks": clocks.summary(),
+        "also": also,
     }
     print(json.dumps(line), flush=True)
+
+
+def mxf4_peak_tflops():
+    """Dense MXF4 tensor peak: the measured bf16 GEMM burst rate times the
+    nominal fp4 : bf16 ratio (13.5 / 2.25 PFLOP/s)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["bf16_tflops"]) * 6.0, "measured bf16 x 6"
+    except (OSError, ValueError, KeyError):
+        return 1900.0 * 6.0, "fallback bf16 x 6"
+
+
+def time_op(fn, flush_l2, stream, reps):
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
+    """Insert throughput and prefill logits / top-k on the 32K-token causal
+    prefill (one sequence, H = 32), each timed alone with a flushed L2."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    hbm, _ = peaks()
+    p = wl.prefill()
+    S = int(p.tok_offsets[-1])
+    cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+    k = bf16_tensor(p.k, dev)
+    slots = torch.from_numpy(p.slots).to(dev)
+    ins_ms = time_op(lambda: idx.quant_insert(k, slots, cache), flush_l2, stream, reps)
+    ins_bytes = S * (256 + 8 + 68)
+    kv, ks = idx.gather_k(cache, torch.from_numpy(p.block_table).to(dev),
+                          torch.from_numpy(p.new_lens.astype(np.int32)).to(dev),
+                          torch.zeros(1, dtype=torch.int64, device=dev), S)
+    qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+    w = torch.from_numpy(p.weights).to(dev)
+    st, en = p.windows()
+    st_d, en_d = torch.from_numpy(st).to(dev), torch.from_numpy(en).to(dev)
+    logits = torch.empty((p.T, S), dtype=torch.float32, device=dev)
+    pre_ms = time_op(lambda: idx.mqa_logits(qv, qs, w, kv, ks, st_d, en_d, p.H, out=logits),
+                     flush_l2, stream, reps)
+    pairs = int((en.astype(np.int64) - st).sum())
+    flops = 2.0 * p.H * 128 * pairs
+    peak_tf, peak_src = mxf4_peak_tflops()
+    out = torch.empty((p.T, TOPK), dtype=torch.int32, device=dev)
+    topk_ms = time_op(lambda: idx.topk_rows(logits, en_d, TOPK, row_start=st_d, out=out),
+                      flush_l2, stream, reps)
+    del logits
+    tf = flops / (pre_ms * 1e-3) / 1e12
+    return {
+        "insert": {"workload": "32768 bf16 keys of the causal prefill", "ms": ins_ms,
+                   "tokens_per_s": S / (ins_ms * 1e-3),
+                   "gbs": ins_bytes / (ins_ms * 1e-3) / 1e9,
+                   "frac_of_hbm": ins_bytes / (ins_ms * 1e-3) / 1e9 / hbm},
+        "prefill_logits": {"workload": "causal 32768 x 32768, H=32 (unclean rows)",
+                           "ms": pre_ms, "tflops": tf, "peak_tflops": peak_tf,
+                           "peak_source": peak_src, "frac": tf / peak_tf,
+                           "store_gbs": pairs * 4 / (pre_ms * 1e-3) / 1e9,
+                           "valid_pairs": pairs},
+        "prefill_topk": {"workload": "32768 causal rows, k=2048", "ms": topk_ms,
+                         "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9},
+    }
 
 
 def cpu_baseline(p, n_seq):

@@ -142,15 +142,20 @@ idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, in
   return IDX_OK;
 }
 
-// Split each sequence's columns [0, cols) into chunks of whole 128-key tiles:
-// about four CTAs per SM over the whole batch, 2..64 tiles per CTA.
-void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms) {
+// Work items for the persistent paged kernels: each sequence's columns
+// [0, cols) are cut into items of whole 128-key tiles, about four items per
+// CTA over the batch (2..64 tiles each), and the grid holds as many CTAs as
+// fit on the device at once (or fewer when there are fewer items).
+void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh) {
+  const int64_t ctas = (int64_t)sms * idx::paged_ctas_per_sm(nh);
   const int64_t tiles = (cols + 127) / 128;
-  int64_t per = (tiles * a.B + 4LL * sms - 1) / (4LL * sms);
+  int64_t per = (tiles * a.B + 4 * ctas - 1) / (4 * ctas);
   per = per < 2 ? 2 : (per > idx::kMaxTilesPerCta ? idx::kMaxTilesPerCta : per);
   a.tiles_per_cta = (int32_t)per;
   const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
   a.chunks = chunks > INT32_MAX ? -1 : (int32_t)chunks;
+  const int64_t items = chunks * a.B;
+  a.grid = (int32_t)(items < ctas ? items : ctas);
 }
 
 }  // namespace
@@ -254,7 +259,7 @@ idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, 
   a.clean = clean ? 1 : 0;
   a.errors = errors;
   const int64_t cap = (int64_t)max_blocks * 64;
-  set_paged_chunking(a, a.clean ? ld : (ld < cap ? ld : cap), sms);
+  set_paged_chunking(a, a.clean ? ld : (ld < cap ? ld : cap), sms, H * next_n);
   if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "ld too large");
   return from_cuda(idx::launch_paged_logits(tv, ts, H, next_n, a, (cudaStream_t)stream),
                    "paged_mqa_logits launch");
@@ -363,7 +368,8 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   a.B = B;
   a.max_blocks = max_blocks;
   a.clean = 0;
-  set_paged_chunking(a, (int64_t)max_blocks * 64, sms);
+  set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n);
+  if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks too large");
   a.topk = k;
   a.out_idx = out_idx;
   a.workspace = workspace;

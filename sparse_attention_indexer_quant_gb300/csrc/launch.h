@@ -30,8 +30,9 @@ struct PagedArgs {
   int32_t B;
   int32_t max_blocks;
   int32_t clean;
-  int32_t tiles_per_cta;  // keys per CTA = 128 * tiles_per_cta
-  int32_t chunks;         // CTAs per sequence
+  int32_t tiles_per_cta;  // keys per work item = 128 * tiles_per_cta
+  int32_t chunks;         // work items per sequence
+  int32_t grid;           // persistent CTAs
   int32_t topk;           // fused only
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only

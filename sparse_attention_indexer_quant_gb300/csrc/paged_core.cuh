@@ -1,6 +1,22 @@
-// Main loop shared by the paged decode kernels (unfused logits and fused
-// logits + top-k): TMA producer, tcgen05 MMA issuer and TMEM epilogue.  The
-// epilogue policy `Ep` decides what happens to each key's dot products.
+// Persistent main loop shared by the paged decode kernels (unfused logits and
+// the scoring half of logits + top-k): each CTA loops over work items
+// (sequence b, chunk of tiles_per_item 128-key tiles) with five warp roles:
+//   warp 0      TMA producer: per tile, two 64x64-byte value boxes (64-byte
+//               swizzle) and two 256-byte scale boxes, gathered by page id,
+//               into a ring of shared-memory stages;
+//   warp 1      MMA issuer: rearranges the tile's 128 key scale words into the
+//               32x16-byte scale-factor layout, tcgen05.cp to TMEM, and two
+//               tcgen05.mma kind::mxf4 block-scaled MMAs (K = 64 each) giving
+//               D[key, j*H + h] in TMEM (fp32);
+//   warps 2-5   epilogue: one thread per key (TMEM lane) loads its row of D and
+//               hands the next_n*H dot products to the epilogue policy `Ep`;
+//   warp 6      item loader: picks the next item (a fixed chunk-major
+//               round-robin, or a global counter when `dynamic`), stages the
+//               sequence's query heads (the MMA's B operand, N = next_n*H), their
+//               scale factors, weights and the chunk's page ids into one of two
+//               buffers, and publishes the item descriptor.
+// The stage ring, the accumulator ring and the two item buffers all run
+// across items, so the TMA stream does not drain between items.
 #pragma once
 
 #include "common.cuh"
@@ -8,37 +24,49 @@
 
 namespace idx {
 
-constexpr int kPagedThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kPagedThreads = 224;
+constexpr int kEpiThreads = 128;
 constexpr int kStages = 6;
-constexpr int kMaxTilesPerCta = 64;
-constexpr int kTileKeys = 128;       // MMA M: two pages
+constexpr int kTileKeys = 128;        // MMA M: two pages
 constexpr int kTileValBytes = kTileKeys * kValBytes;  // 8192
+constexpr int kMaxTilesPerCta = 64;   // tiles per work item
 
 __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
 }
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// CTAs per SM the persistent grid is sized for: two, except for N = 128 whose
+// epilogue needs the registers of a whole SM.
+__host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 128 ? 1 : 2; }
+
+struct ItemDesc {
+  int64_t L;        // context length after validation
+  int64_t k0;       // first key of the item
+  int64_t k_end;    // end of the item's column range
+  int32_t b;        // sequence
+  int32_t n_tiles;  // tiles holding a key < L; -1 ends the item stream
+};
+
 // Shared-memory and tensor-memory plan for N = NH query-head columns.
 template <int NH>
 struct PagedLayout {
-  // accumulator buffers: as many as keep a CTA within 128 TMEM columns (N = 32,
-  // 64) or 256 columns (N = 128), so that 2-4 CTAs share an SM
-  static constexpr int kAccBufs = NH == 32 ? 3 : 1;
-  static constexpr uint32_t kSfbCol = kAccBufs * NH;     // 4 columns
-  static constexpr uint32_t kSfaCol = kSfbCol + 4;       // 4 columns per accumulator
+  static constexpr int kAccBufs = NH == 32 ? 4 : 2;
+  static constexpr uint32_t kSfbCol = kAccBufs * NH;        // 2 x 4 columns
+  static constexpr uint32_t kSfaCol = kSfbCol + 8;          // 4 columns per accumulator
   static constexpr uint32_t kTmemCols = tmem_cols_for(kSfaCol + 4 * kAccBufs);
-  static constexpr size_t kA = 0;                                   // stages x 8192 (SW64)
-  static constexpr size_t kB = kA + (size_t)kStages * kTileValBytes; // NH x 64 (SW64)
-  static constexpr size_t kSfRaw = kB + (size_t)NH * kValBytes;      // stages x 512
-  static constexpr size_t kSfa = kSfRaw + (size_t)kStages * 512;     // stages x 512
-  static constexpr size_t kSfb = kSfa + (size_t)kStages * 512;       // 512
-  static constexpr size_t kW = kSfb + 512;                           // NH floats
-  static constexpr size_t kBt = kW + (size_t)NH * 4;                 // 2 x 64 page ids
-  static constexpr size_t kBars = align_up(kBt + 2 * kMaxTilesPerCta * 4, 16);
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs;
-  static constexpr size_t kMisc = kBars + (size_t)kNumBars * 8;      // tmem base, abort
-  static constexpr size_t kExtra = align_up(kMisc + 16, 1024);       // epilogue's region
+  static constexpr size_t kA = 0;                                      // stages x 8192 (SW64)
+  static constexpr size_t kB = kA + (size_t)kStages * kTileValBytes;   // 2 x NH x 64 (SW64)
+  static constexpr size_t kSfRaw = kB + 2 * (size_t)NH * kValBytes;    // stages x 512
+  static constexpr size_t kSfa = kSfRaw + (size_t)kStages * 512;       // stages x 512
+  static constexpr size_t kSfb = kSfa + (size_t)kStages * 512;         // 2 x 512
+  static constexpr size_t kW = kSfb + 2 * 512;                         // 2 x NH floats
+  static constexpr size_t kBt = kW + 2 * (size_t)NH * 4;               // 2 x 128 page ids
+  static constexpr size_t kItem = align_up(kBt + 2 * 2 * kMaxTilesPerCta * 4, 16);
+  static constexpr size_t kBars = kItem + 2 * sizeof(ItemDesc);
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4;
+  static constexpr size_t kMisc = kBars + (size_t)kNumBars * 8;        // tmem base, abort
+  static constexpr size_t kExtra = align_up(kMisc + 16, 1024);         // epilogue's region
 };
 
 template <int NH>
@@ -46,41 +74,25 @@ __host__ __device__ constexpr size_t paged_smem_bytes() {
   return PagedLayout<NH>::kExtra + 1024;  // + slack to align the base to 1024
 }
 
-struct PagedCta {
-  int b;
-  int64_t L;        // context length after validation
-  int64_t k0;       // first key of this CTA's chunk
-  int64_t k_end;    // end of the chunk's column range
-  int n_tiles;      // tiles of 128 keys holding at least one key < L
-};
-
-__device__ __forceinline__ bool paged_cta_setup(const PagedArgs& p, PagedCta& c) {
-  c.b = blockIdx.y;
-  const int64_t chunk_keys = (int64_t)p.tiles_per_cta * kTileKeys;
-  c.k0 = (int64_t)blockIdx.x * chunk_keys;
-  c.k_end = c.k0 + chunk_keys;
-  int64_t L = __ldg(p.context_lens + c.b);
+// Work item w in chunk-major order: w = c * B + b.
+__device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, bool count_errors) {
+  ItemDesc it;
+  it.b = (int32_t)(w % p.B);
+  const int64_t c = w / p.B;
+  const int64_t C = (int64_t)p.tiles_per_cta * kTileKeys;
+  it.k0 = c * C;
+  it.k_end = it.k0 + C;
+  int64_t L = __ldg(p.context_lens + it.b);
   int64_t cap = (int64_t)p.max_blocks * kPage;
   if (p.logits != nullptr && p.ld < cap) cap = p.ld;
   if (L < 0 || L > cap) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) count_bad_input(p.errors);
+    if (count_errors && c == 0) count_bad_input(p.errors);
     L = L < 0 ? 0 : cap;
   }
-  c.L = L;
-  const int64_t k1 = L < c.k_end ? L : c.k_end;
-  c.n_tiles = k1 > c.k0 ? (int)((k1 - c.k0 + kTileKeys - 1) / kTileKeys) : 0;
-  return c.n_tiles > 0;
-}
-
-// -inf into the columns of this CTA's chunk that no tile covers.
-template <int NEXT_N>
-__device__ __forceinline__ void clean_tail(const PagedArgs& p, const PagedCta& c) {
-  const int64_t lo = c.k0 + (int64_t)c.n_tiles * kTileKeys;
-  const int64_t hi = c.k_end < p.ld ? c.k_end : p.ld;
-  for (int j = 0; j < NEXT_N; ++j) {
-    float* row = p.logits + ((int64_t)c.b * NEXT_N + j) * p.ld;
-    for (int64_t s = lo + threadIdx.x; s < hi; s += blockDim.x) row[s] = -INFINITY;
-  }
+  it.L = L;
+  const int64_t k1 = L < it.k_end ? L : it.k_end;
+  it.n_tiles = k1 > it.k0 ? (int32_t)((k1 - it.k0 + kTileKeys - 1) / kTileKeys) : 0;
+  return it;
 }
 
 // out[j] = sum_h w[j*H + h] * max(0, d[j*H + h]), h ascending.
@@ -108,10 +120,16 @@ __device__ __forceinline__ uint8_t* aligned_smem_base() {
   return smem_raw + ((1024u - (a & 1023u)) & 1023u);
 }
 
+// Barrier among the four epilogue warps only.
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
 template <int H, int NEXT_N, class Ep>
-__device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
-                                              const CUtensorMap* tm_scales, const PagedArgs& p,
-                                              const PagedCta& c) {
+__device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
+                                                     const CUtensorMap* tm_scales,
+                                                     const PagedArgs& p, bool dynamic,
+                                                     bool pass_empty, uint32_t* item_counter) {
   constexpr int NH = H * NEXT_N;
   using Lay = PagedLayout<NH>;
   constexpr int ACC = Lay::kAccBufs;
@@ -124,20 +142,22 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
   uint8_t* sSfa = sm + Lay::kSfa;
   uint8_t* sSfb = sm + Lay::kSfb;
   float* sW = reinterpret_cast<float*>(sm + Lay::kW);
+  int32_t* sBt = reinterpret_cast<int32_t*>(sm + Lay::kBt);
+  ItemDesc* sItem = reinterpret_cast<ItemDesc*>(sm + Lay::kItem);
   const uint32_t bars = smem_u32(sm + Lay::kBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto tfull_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bars + 8u * (2 * kStages + ACC + a); };
+  auto qfull_bar = [&](int q) { return bars + 8u * (2 * kStages + 2 * ACC + q); };
+  auto qempty_bar = [&](int q) { return bars + 8u * (2 * kStages + 2 * ACC + 2 + q); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::kMisc + 4);
   uint8_t* extra = sm + Lay::kExtra;
-  int32_t* sBt = reinterpret_cast<int32_t*>(sm + Lay::kBt);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // ---- setup: TMEM, barriers, the sequence's query heads and weights
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
     tmem_relinquish();
@@ -151,71 +171,122 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 4);
     }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(qfull_bar(q), 1);
+      mbar_init(qempty_bar(q), 1 + 4);  // the MMA commit + the four epilogue warps
+    }
     *abort = 0;
     fence_mbar_init();
   }
-  {
-    // B operand: row n = j*H + h of this sequence's query heads, 64 bytes,
-    // stored with the 64-byte swizzle (16-byte chunk c of row n at chunk
-    // c ^ ((n >> 1) & 3)).
-    const uint8_t* qv = p.q_vals + (int64_t)c.b * NH * kValBytes;
-    for (int i = threadIdx.x; i < NH * 4; i += kPagedThreads) {
-      const int n = i >> 2, ch = i & 3;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qv + n * kValBytes) + ch);
-      *reinterpret_cast<uint4*>(sB + n * kValBytes + ((ch ^ ((n >> 1) & 3)) << 4)) = v;
-    }
-    // B scale factors in the 32x16-byte atom: row n's 4 bytes at
-    // 16*(n % 32) + 4*(n / 32); rows past NH are zero.
-    const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)c.b * NH;
-    for (int n = threadIdx.x; n < 128; n += kPagedThreads) {
-      const uint32_t wv = n < NH ? __ldg(qs + n) : 0u;
-      *reinterpret_cast<uint32_t*>(sSfb + 16 * (n % 32) + 4 * (n / 32)) = wv;
-    }
-    for (int n = threadIdx.x; n < NH; n += kPagedThreads)
-      sW[n] = __ldg(p.weights + (int64_t)c.b * NH + n);
-    // the chunk's page ids; pages past the context are not read
-    const int32_t* bt = p.block_table + (int64_t)c.b * p.max_blocks + c.k0 / kPage;
-    const int n_pages = (int)((c.L - c.k0 + kPage - 1) / kPage);
-    for (int i = threadIdx.x; i < 2 * c.n_tiles; i += kPagedThreads)
-      sBt[i] = i < n_pages ? __ldg(bt + i) : 0;
-    Ep::init(extra);
-  }
-  fence_proxy_async_smem();
+  Ep::init(extra);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int64_t n_items = (int64_t)p.B * p.chunks;
 
-  if (warp == 0) {
+  if (warp == 6) {
+    // ---------------------------------------------------------- item loader
+    int n = 0;
+    int64_t w = dynamic ? -1 : (int64_t)blockIdx.x - (int64_t)gridDim.x;
+    while (true) {
+      ItemDesc it;
+      it.n_tiles = -1;
+      // the next item with work (with pass_empty: the next item)
+      while (true) {
+        if (dynamic) {
+          uint32_t t = 0;
+          if (lane == 0) t = atomicAdd(item_counter, 1u);
+          w = (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
+        } else {
+          w += gridDim.x;
+        }
+        if (w >= n_items) {
+          it.n_tiles = -1;
+          break;
+        }
+        it = paged_item(p, w, lane == 0);
+        if (it.n_tiles > 0 || pass_empty) break;
+      }
+      const int qb = n & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(qempty_bar(qb), ((n >> 1) & 1) ^ 1, abort))) {
+        if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);
+        break;
+      }
+      if (it.n_tiles > 0) {
+        // B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
+        // stored with the 64-byte swizzle (16-byte chunk c of row r at chunk
+        // c ^ ((r >> 1) & 3)); its scale factors in the 32x16-byte atom (row
+        // r's 4 bytes at 16*(r % 32) + 4*(r / 32), rows past NH zero).
+        uint8_t* b_dst = sB + (size_t)qb * NH * kValBytes;
+        const uint8_t* qv = p.q_vals + (int64_t)it.b * NH * kValBytes;
+        for (int i = lane; i < NH * 4; i += 32) {
+          const int r = i >> 2, ch = i & 3;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qv + r * kValBytes) + ch);
+          *reinterpret_cast<uint4*>(b_dst + r * kValBytes + ((ch ^ ((r >> 1) & 3)) << 4)) = v;
+        }
+        const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)it.b * NH;
+        for (int r = lane; r < 128; r += 32) {
+          const uint32_t wv = r < NH ? __ldg(qs + r) : 0u;
+          *reinterpret_cast<uint32_t*>(sSfb + qb * 512 + 16 * (r % 32) + 4 * (r / 32)) = wv;
+        }
+        for (int r = lane; r < NH; r += 32)
+          sW[qb * NH + r] = __ldg(p.weights + (int64_t)it.b * NH + r);
+        const int32_t* bt = p.block_table + (int64_t)it.b * p.max_blocks + it.k0 / kPage;
+        const int n_pages = (int)((it.L - it.k0 + kPage - 1) / kPage);
+        for (int i = lane; i < 2 * it.n_tiles; i += 32)
+          sBt[qb * 2 * kMaxTilesPerCta + i] = i < n_pages ? __ldg(bt + i) : 0;
+      }
+      if (lane == 0) sItem[qb] = it;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qfull_bar(qb));
+      ++n;
+      if (it.n_tiles < 0) break;
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
+    int issued = 0;
     if (lane == 0) {
       tma_prefetch_desc(tm_vals);
       tma_prefetch_desc(tm_scales);
-      int issued = 0;
-      for (int i = 0; i < c.n_tiles; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(empty_bar(s), ((i / kStages) & 1) ^ 1, abort)) {
+      for (int n = 0;; ++n) {
+        const int qb = n & 1;
+        if (!mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort)) {
           flag_timeout(p.errors, kTimeoutProducer);
           break;
         }
-        const bool two = c.k0 + (int64_t)(2 * i + 1) * kPage < c.L;
-        const int32_t id0 = sBt[2 * i];
-        const int32_t id1 = sBt[2 * i + 1];
-        // out-of-range ids load the TMA fill (zeros) instead of faulting
-        if (id0 < 0 || id0 >= p.num_blocks) count_bad_input(p.errors);
-        if (two && (id1 < 0 || id1 >= p.num_blocks)) count_bad_input(p.errors);
-        const uint32_t bytes = (two ? 2u : 1u) * (kPageValBytes + 256u);
-        const uint32_t fb = full_bar(s);
-        mbar_arrive_expect_tx(fb, bytes);
-        const uint32_t a_dst = smem_u32(sA + (size_t)s * kTileValBytes);
-        const uint32_t sf_dst = smem_u32(sSfRaw + (size_t)s * 512);
-        tma_load_3d(a_dst, tm_vals, 0, 0, id0, fb);
-        tma_load_2d(sf_dst, tm_scales, 0, id0, fb);
-        if (two) {
-          tma_load_3d(a_dst + kPageValBytes, tm_vals, 0, 0, id1, fb);
-          tma_load_2d(sf_dst + 256, tm_scales, 0, id1, fb);
+        const ItemDesc it = sItem[qb];
+        if (it.n_tiles < 0) break;
+        const int32_t* ids = sBt + qb * 2 * kMaxTilesPerCta;
+        bool ok = true;
+        for (int t = 0; t < it.n_tiles; ++t) {
+          const int s = issued % kStages;
+          if (!mbar_wait(empty_bar(s), ((issued / kStages) & 1) ^ 1, abort)) {
+            flag_timeout(p.errors, kTimeoutProducer);
+            ok = false;
+            break;
+          }
+          const bool two = it.k0 + (int64_t)(2 * t + 1) * kPage < it.L;
+          const int32_t id0 = ids[2 * t];
+          const int32_t id1 = ids[2 * t + 1];
+          // out-of-range ids load the TMA fill (zeros) instead of faulting
+          if (id0 < 0 || id0 >= p.num_blocks) count_bad_input(p.errors);
+          if (two && (id1 < 0 || id1 >= p.num_blocks)) count_bad_input(p.errors);
+          const uint32_t bytes = (two ? 2u : 1u) * (kPageValBytes + 256u);
+          const uint32_t fb = full_bar(s);
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t a_dst = smem_u32(sA + (size_t)s * kTileValBytes);
+          const uint32_t sf_dst = smem_u32(sSfRaw + (size_t)s * 512);
+          tma_load_3d(a_dst, tm_vals, 0, 0, id0, fb);
+          tma_load_2d(sf_dst, tm_scales, 0, id0, fb);
+          if (two) {
+            tma_load_3d(a_dst + kPageValBytes, tm_vals, 0, 0, id1, fb);
+            tma_load_2d(sf_dst + 256, tm_scales, 0, id1, fb);
+          }
+          ++issued;
         }
-        ++issued;
+        if (!ok) break;
       }
       // every copy this thread issued must land before the CTA can exit
       for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
@@ -224,74 +295,108 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    const uint32_t sfb_t = tmem + Lay::kSfbCol;
-    if (lane == 0) tmem_cp_32x128b_x4(sfb_t, smem_desc(smem_u32(sSfb), 16, 128, kLayoutNone));
-    __syncwarp();
-    const uint64_t b_desc = smem_desc(smem_u32(sB), 16, 512, kLayoutSw64);
-    int issued = 0;
-    for (int i = 0; i < c.n_tiles; ++i) {
-      const int s = i % kStages;
-      const int a = i % ACC;
-      const bool ok = mbar_wait(full_bar(s), (i / kStages) & 1, abort) &&
-                      mbar_wait(tempty_bar(a), ((i / ACC) & 1) ^ 1, abort);
-      if (!ok) {
+    int tiles = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int qb = n & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort))) {
         if (lane == 0) flag_timeout(p.errors, kTimeoutMma);
         break;
       }
+      const ItemDesc it = sItem[qb];
+      if (it.n_tiles < 0) break;
       tc_fence_after();
-      // scale-factor atom: row l holds the 4-byte scale words of tile keys
-      // l, l+32, l+64, l+96 (key k's word is word k of the two pages' scale
-      // areas as loaded)
-      const uint32_t* raw = reinterpret_cast<const uint32_t*>(sSfRaw + (size_t)s * 512);
-      const uint4 row = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
-      *reinterpret_cast<uint4*>(sSfa + (size_t)s * 512 + 16 * lane) = row;
-      fence_proxy_async_smem();
+      const uint32_t sfb_t = tmem + Lay::kSfbCol + 4u * qb;
+      if (lane == 0 && it.n_tiles > 0)
+        tmem_cp_32x128b_x4(sfb_t, smem_desc(smem_u32(sSfb + qb * 512), 16, 128, kLayoutNone));
       __syncwarp();
-      if (lane == 0) {
-        const uint32_t sfa_t = tmem + Lay::kSfaCol + 4u * a;
-        tmem_cp_32x128b_x4(sfa_t,
-                           smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
-        const uint32_t d_t = tmem + (uint32_t)(a * NH);
-        const uint64_t a_desc =
-            smem_desc(smem_u32(sA + (size_t)s * kTileValBytes), 16, 512, kLayoutSw64);
-        // K = 0..63 uses scale bytes 0,1 of each row; K = 64..127 bytes 2,3.
-        // The second half of each 64-byte row starts 32 bytes in (+2 in the
-        // descriptor's 16-byte units).
-        mma_mxf4(d_t, a_desc, b_desc, mxf4_idesc(NH, 0, 0), sfa_t, sfb_t, 0u);
-        mma_mxf4(d_t, a_desc + 2, b_desc + 2, mxf4_idesc(NH, 2, 2), sfa_t, sfb_t, 1u);
-        mma_commit(empty_bar(s));
-        mma_commit(tfull_bar(a));
+      const uint64_t b_desc =
+          smem_desc(smem_u32(sB + (size_t)qb * NH * kValBytes), 16, 512, kLayoutSw64);
+      for (int t = 0; t < it.n_tiles; ++t) {
+        const int s = tiles % kStages;
+        const int a = tiles % ACC;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), (tiles / kStages) & 1, abort) &&
+                                         mbar_wait(tempty_bar(a), ((tiles / ACC) & 1) ^ 1, abort));
+        if (!ok) {
+          if (lane == 0) flag_timeout(p.errors, kTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        // scale-factor atom: row l holds the 4-byte scale words of tile keys
+        // l, l+32, l+64, l+96 (key k's word is word k of the two pages' scale
+        // areas as loaded)
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(sSfRaw + (size_t)s * 512);
+        const uint4 row = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
+        *reinterpret_cast<uint4*>(sSfa + (size_t)s * 512 + 16 * lane) = row;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t sfa_t = tmem + Lay::kSfaCol + 4u * a;
+          tmem_cp_32x128b_x4(sfa_t,
+                             smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
+          const uint32_t d_t = tmem + (uint32_t)(a * NH);
+          const uint64_t a_desc =
+              smem_desc(smem_u32(sA + (size_t)s * kTileValBytes), 16, 512, kLayoutSw64);
+          // K = 0..63 uses scale bytes 0,1 of each row; K = 64..127 bytes 2,3.
+          // The second half of each 64-byte row starts 32 bytes in (+2 in the
+          // descriptor's 16-byte units).
+          mma_mxf4(d_t, a_desc, b_desc, mxf4_idesc(NH, 0, 0), sfa_t, sfb_t, 0u);
+          mma_mxf4(d_t, a_desc + 2, b_desc + 2, mxf4_idesc(NH, 2, 2), sfa_t, sfb_t, 1u);
+          mma_commit(empty_bar(s));
+          mma_commit(tfull_bar(a));
+        }
+        __syncwarp();
+        ++tiles;
       }
+      // the item's B buffer is free once its MMAs are done
+      if (lane == 0) mma_commit(qempty_bar(qb));
       __syncwarp();
-      ++issued;
     }
     // the last MMAs must have finished before TMEM is released
-    if (lane == 0 && issued > 0) {
-      const int i = issued - 1;
+    if (lane == 0 && tiles > 0) {
+      const int i = tiles - 1;
       if (!mbar_wait_drain(tfull_bar(i % ACC), (i / ACC) & 1))
         flag_timeout(p.errors, kTimeoutDrain);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int m = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    for (int i = 0; i < c.n_tiles; ++i) {
-      const int a = i % ACC;
-      if (!mbar_wait(tfull_bar(a), (i / ACC) & 1, abort)) {
-        if (lane == 0) flag_timeout(p.errors, kTimeoutEpilogue);
-        break;
-      }
-      tc_fence_after();
-      float d[NH];
+    int tiles = 0;
+    for (int n = 0;; ++n) {
+      const int qb = n & 1;
+      // every epilogue warp takes the same branches: a wait that gives up
+      // raises *abort, the item loop still runs to its end (later waits return
+      // at once), and the four warps leave together after the barrier
+      const bool have = __all_sync(0xFFFFFFFFu, mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort));
+      const ItemDesc it = sItem[qb];
+      const bool stop = !have || it.n_tiles < 0;
+      const int n_tiles = stop ? 0 : it.n_tiles;
+      const float* w = sW + qb * NH;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int a = tiles % ACC;
+        ++tiles;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull_bar(a), ((tiles - 1) / ACC) & 1, abort))) {
+          if (lane == 0) flag_timeout(p.errors, kTimeoutEpilogue);
+          continue;
+        }
+        tc_fence_after();
+        float d[NH];
 #pragma unroll
-      for (int part = 0; part < NH / 32; ++part)
-        tmem_ld32_sync(lane_addr + (uint32_t)(a * NH + 32 * part),
-                       *reinterpret_cast<float(*)[32]>(&d[32 * part]));
-      tc_fence_before();
+        for (int part = 0; part < NH / 32; ++part)
+          tmem_ld32_sync(lane_addr + (uint32_t)(a * NH + 32 * part),
+                         *reinterpret_cast<float(*)[32]>(&d[32 * part]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(a));
+        Ep::tile(p, it, w, extra, it.k0 + (int64_t)t * kTileKeys + m, d);
+      }
+      epilogue_sync();
+      if (stop || *abort) break;
+      Ep::item_done(p, it, extra);
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(a));
-      Ep::tile(p, c, sW, extra, c.k0 + (int64_t)i * kTileKeys + m, d);
+      if (lane == 0) mbar_arrive(qempty_bar(qb));
     }
   }
 
@@ -301,8 +406,6 @@ __device__ __forceinline__ void paged_cta_run(const CUtensorMap* tm_vals,
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kTmemCols);
   }
-  const bool ok = *abort == 0;
-  Ep::chunk_done(p, c, extra, ok);
 }
 
 }  // namespace idx

@@ -4,19 +4,10 @@
 // MQA-logits reader), computing for query row r = (b, j)
 //     logit[r, s] = sum_h w[r, h] * max(0, q^[r, h] . k^[s]).
 //
-// One CTA scores a chunk of one sequence's context, 128 keys (two pages) per
-// tile, with three warp roles:
-//   warp 0      TMA producer: reads the block table and issues, per tile, two
-//               64x64-byte value boxes (64-byte swizzle) and two 256-byte scale
-//               boxes, gathered by page id, into a ring of shared-memory stages;
-//   warp 1      MMA issuer: rearranges the tile's 128 scale words into the
-//               32x16-byte scale-factor layout, copies it to tensor memory with
-//               tcgen05.cp, and issues two tcgen05.mma kind::mxf4 block-scaled
-//               MMAs (K = 64 each): D[key, j*H + h] in TMEM, fp32;
-//   warps 2-5   epilogue: one thread per key (TMEM lane) loads its row of D and
-//               forms sum_h w * max(0, D) for each of the next_n query rows.
-// The query heads of the sequence (the MMA's B operand, N = next_n * H rows)
-// and their scale factors are staged once per CTA.
+// The persistent main loop of paged_core.cuh streams each sequence's pages
+// through tcgen05 block-scaled MXF4 MMAs; this file's epilogue forms
+// sum_h w * max(0, D) for each of the next_n query rows of a key and writes it
+// to the logits row (-inf past the window when the rows are clean).
 #include <math.h>
 
 #include "common.cuh"
@@ -34,36 +25,42 @@ struct UnfusedEpilogue {
 
   // Called once per tile by every epilogue thread with its key's NH dot
   // products (column n = j*H + h).
-  __device__ __forceinline__ static void tile(const PagedArgs& p, const PagedCta& c,
+  __device__ __forceinline__ static void tile(const PagedArgs& p, const ItemDesc& it,
                                               const float* w_smem, uint8_t* /*extra*/,
                                               int64_t key, const float (&d)[NH]) {
     float logit[NEXT_N];
     weighted_relu_sum<H, NEXT_N>(w_smem, d, logit);
 #pragma unroll
     for (int j = 0; j < NEXT_N; ++j) {
-      const int64_t len = c.L - NEXT_N + j + 1;
-      float* row = p.logits + ((int64_t)c.b * NEXT_N + j) * p.ld;
+      const int64_t len = it.L - NEXT_N + j + 1;
+      float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
       if (key < len)
         row[key] = logit[j];
       else if (p.clean && key < p.ld)
         row[key] = -INFINITY;
     }
   }
-  __device__ __forceinline__ static void chunk_done(const PagedArgs&, const PagedCta&, uint8_t*,
-                                                    bool) {}
+
+  // -inf into the item's columns that no tile covered (clean rows only).
+  __device__ __forceinline__ static void item_done(const PagedArgs& p, const ItemDesc& it,
+                                                   uint8_t*) {
+    if (!p.clean) return;
+    const int64_t lo = it.k0 + (int64_t)it.n_tiles * kTileKeys;
+    const int64_t hi = it.k_end < p.ld ? it.k_end : p.ld;
+    const int e = threadIdx.x - 2 * 32;  // epilogue threads are warps 2-5
+    for (int j = 0; j < NEXT_N; ++j) {
+      float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
+      for (int64_t s = lo + e; s < hi; s += kEpiThreads) row[s] = -INFINITY;
+    }
+  }
 };
 
 template <int H, int NEXT_N>
-__global__ void __launch_bounds__(kPagedThreads, 1)
+__global__ void __launch_bounds__(kPagedThreads, paged_ctas_per_sm(H * NEXT_N))
     paged_logits_kernel(const __grid_constant__ CUtensorMap tm_vals,
                         const __grid_constant__ CUtensorMap tm_scales, const PagedArgs p) {
-  PagedCta c;
-  if (!paged_cta_setup(p, c)) {
-    if (p.clean) clean_tail<NEXT_N>(p, c);
-    return;
-  }
-  if (p.clean) clean_tail<NEXT_N>(p, c);
-  paged_cta_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>>(&tm_vals, &tm_scales, p, c);
+  paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>>(&tm_vals, &tm_scales, p, false,
+                                                              p.clean != 0, nullptr);
 }
 
 template <int H, int NEXT_N>
@@ -75,8 +72,7 @@ cudaError_t launch_one(const CUtensorMap& tv, const CUtensorMap& ts, const Paged
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)a.chunks, (unsigned)a.B);
-  kern<<<grid, kPagedThreads, smem, stream>>>(tv, ts, a);
+  kern<<<(unsigned)a.grid, kPagedThreads, smem, stream>>>(tv, ts, a);
   return cudaGetLastError();
 }
 

@@ -3,11 +3,12 @@
 // launches that hand the logits over through the caller's workspace instead of
 // a logits tensor:
 //
-//   1. score    the shared TMA + tcgen05 main loop; the epilogue stores each
-//               valid logit to the workspace (a row-major scratch that stays in
-//               L2 for these sizes) and adds it to a shared-memory coarse
-//               histogram (top 12 key bits) of its row; each CTA folds its
-//               histograms into the row's global histogram at the end.
+//   1. score    the persistent TMA + tcgen05 main loop (work items taken from
+//               a counter in the workspace); the epilogue stores each valid
+//               logit to the workspace (a row-major scratch that stays in L2 for
+//               these sizes) and adds it to a shared-memory coarse histogram
+//               (top 12 key bits) of its row, folded into the row's global
+//               histogram at the end of each item.
 //   2. select   grid (segment of 8192 keys, row).  Every CTA finds from the
 //               row histogram the bin that holds the row's k-th largest logit,
 //               writes the positions of its segment's logits above that bin
@@ -16,7 +17,8 @@
 //               remainder from that list.
 //
 // Workspace (device, caller-owned, 256-byte aligned pieces):
-//   u32 hist[rows][4096] and u32 ctr[rows][4] (zeroed by a memset per call)
+//   u32 hist[rows][4096], u32 ctr[rows][4], u32 item counter (zeroed by a
+//   memset per call)
 //   f32 logits[rows][ldw], u32 bkeys[rows][ldw], i32 bpos[rows][ldw]
 #include <math.h>
 
@@ -31,10 +33,12 @@ namespace {
 constexpr int kSelThreads = 256;
 constexpr int kSegKeys = 8192;
 constexpr int kSelCap = 4096;
+constexpr int kPerThread = kSegKeys / kSelThreads;  // 32
 
 struct TopkWs {
   uint32_t* hist;     // [rows][kCoarseBins]
   uint32_t* ctr;      // [rows][4]: slot, boundary count, ticket, unused
+  uint32_t* items;    // work-item counter of the scoring pass
   float* logits;      // [rows][ldw]
   uint32_t* bkeys;    // [rows][ldw]
   int32_t* bpos;      // [rows][ldw]
@@ -48,12 +52,13 @@ __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t ma
                                             size_t* total) {
   const int64_t ldw = (int64_t)max_blocks * kPage;
   const size_t h = ws_align((size_t)rows * kCoarseBins * 4);
-  const size_t c = ws_align((size_t)rows * 16);
+  const size_t c = ws_align((size_t)rows * 16 + 4);
   const size_t e = ws_align((size_t)rows * ldw * 4);
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
   w.hist = reinterpret_cast<uint32_t*>(p);
   w.ctr = reinterpret_cast<uint32_t*>(p + h);
+  w.items = reinterpret_cast<uint32_t*>(p + h) + rows * 4;
   w.logits = reinterpret_cast<float*>(p + h + c);
   w.bkeys = reinterpret_cast<uint32_t*>(p + h + c + e);
   w.bpos = reinterpret_cast<int32_t*>(p + h + c + 2 * e);
@@ -73,7 +78,7 @@ struct ScoreEpilogue {
     for (int i = threadIdx.x; i < NEXT_N * kCoarseBins; i += blockDim.x) h[i] = 0;
   }
 
-  __device__ __forceinline__ static void tile(const PagedArgs& p, const PagedCta& c,
+  __device__ __forceinline__ static void tile(const PagedArgs& p, const ItemDesc& it,
                                               const float* w_smem, uint8_t* extra, int64_t key,
                                               const float (&d)[NH]) {
     uint32_t* hist = reinterpret_cast<uint32_t*>(extra);
@@ -82,35 +87,42 @@ struct ScoreEpilogue {
     weighted_relu_sum<H, NEXT_N>(w_smem, d, logit);
 #pragma unroll
     for (int j = 0; j < NEXT_N; ++j) {
-      const int64_t len = c.L - NEXT_N + j + 1;
+      const int64_t len = it.L - NEXT_N + j + 1;
       const bool valid = key < len;
-      const int64_t r = (int64_t)c.b * NEXT_N + j;
+      const int64_t r = (int64_t)it.b * NEXT_N + j;
       if (valid) ws.logits[r * ws.ldw + key] = logit[j];
       hist_add(hist + j * kCoarseBins, coarse_bin(float_key(logit[j])), valid);
     }
   }
 
-  __device__ __forceinline__ static void chunk_done(const PagedArgs& p, const PagedCta& c,
-                                                    uint8_t* extra, bool) {
-    const uint32_t* hist = reinterpret_cast<const uint32_t*>(extra);
+  // Folds the item's histograms into its rows' global histograms and clears
+  // them for the next item (the four epilogue warps, after their last tile).
+  __device__ __forceinline__ static void item_done(const PagedArgs& p, const ItemDesc& it,
+                                                   uint8_t* extra) {
+    uint32_t* hist = reinterpret_cast<uint32_t*>(extra);
     const TopkWs ws = ws_layout(p.workspace, (int64_t)p.B * NEXT_N, p.max_blocks, nullptr);
+    const int e = threadIdx.x - 2 * 32;  // epilogue threads are warps 2-5
     for (int j = 0; j < NEXT_N; ++j) {
-      uint32_t* g = ws.hist + ((int64_t)c.b * NEXT_N + j) * kCoarseBins;
-      for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) {
+      uint32_t* g = ws.hist + ((int64_t)it.b * NEXT_N + j) * kCoarseBins;
+      for (int i = e; i < kCoarseBins; i += kEpiThreads) {
         const uint32_t v = hist[j * kCoarseBins + i];
-        if (v) atomicAdd(g + i, v);
+        if (v) {
+          atomicAdd(g + i, v);
+          hist[j * kCoarseBins + i] = 0;
+        }
       }
     }
+    epilogue_sync();
   }
 };
 
 template <int H, int NEXT_N>
-__global__ void __launch_bounds__(kPagedThreads, 1)
+__global__ void __launch_bounds__(kPagedThreads, paged_ctas_per_sm(H * NEXT_N))
     paged_score_kernel(const __grid_constant__ CUtensorMap tm_vals,
                        const __grid_constant__ CUtensorMap tm_scales, const PagedArgs p) {
-  PagedCta c;
-  if (!paged_cta_setup(p, c)) return;
-  paged_cta_run<H, NEXT_N, ScoreEpilogue<H, NEXT_N>>(&tm_vals, &tm_scales, p, c);
+  const TopkWs ws = ws_layout(p.workspace, (int64_t)p.B * NEXT_N, p.max_blocks, nullptr);
+  paged_persistent_run<H, NEXT_N, ScoreEpilogue<H, NEXT_N>>(&tm_vals, &tm_scales, p, true, false,
+                                                            ws.items);
 }
 
 struct SelectSmem {
@@ -120,6 +132,8 @@ struct SelectSmem {
   uint32_t ticket;
   uint32_t slot;
   uint32_t slot_fill;
+  uint32_t base_above;
+  uint32_t base_bnd;
 };
 
 __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedArgs p,
@@ -158,17 +172,44 @@ __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedAr
   const float* x = ws.logits + r * ws.ldw;
   uint32_t* bkeys = ws.bkeys + r * ws.ldw;
   int32_t* bpos = ws.bpos + r * ws.ldw;
-  const GlobalLogits<true> seg{x, lo, hi};
-  seg.for_each([&](uint32_t key, int32_t i) {
+  // this thread's logits of the segment, all loads in flight together
+  float v[kPerThread];
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t i = lo + (int64_t)u * kSelThreads + threadIdx.x;
+    v[u] = i < hi ? __ldcg(x + i) : 0.f;
+  }
+  uint32_t n_above = 0, n_bnd = 0;
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t i = lo + (int64_t)u * kSelThreads + threadIdx.x;
+    const uint32_t bin = coarse_bin(float_key(v[u]));
+    n_above += (i < hi && bin > b1) ? 1u : 0u;
+    n_bnd += (i < hi && bin == b1) ? 1u : 0u;
+  }
+  // one block scan and one global claim per counter for the whole CTA
+  const uint32_t packed = (n_above << 16) | n_bnd;
+  const uint32_t excl = block_exclusive_scan(packed, sm.sel.s);
+  if (threadIdx.x == blockDim.x - 1) {
+    const uint32_t tot = excl + packed;
+    sm.base_above = (tot >> 16) ? atomicAdd(ctr + 0, tot >> 16) : 0u;
+    sm.base_bnd = (tot & 0xFFFFu) ? atomicAdd(ctr + 1, tot & 0xFFFFu) : 0u;
+  }
+  __syncthreads();
+  uint32_t a_slot = sm.base_above + (excl >> 16);
+  uint32_t b_slot = sm.base_bnd + (excl & 0xFFFFu);
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t i = lo + (int64_t)u * kSelThreads + threadIdx.x;
+    const uint32_t key = float_key(v[u]);
     const uint32_t bin = coarse_bin(key);
-    const uint32_t slot = warp_claim(ctr + 0, bin > b1);
-    if (bin > b1) orow[slot] = i;
-    const uint32_t bs = warp_claim(ctr + 1, bin == b1);
-    if (bin == b1) {
-      bkeys[bs] = key;
-      bpos[bs] = i;
+    if (i < hi && bin > b1) orow[a_slot++] = (int32_t)i;
+    if (i < hi && bin == b1) {
+      bkeys[b_slot] = key;
+      bpos[b_slot] = (int32_t)i;
+      ++b_slot;
     }
-  });
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) sm.ticket = atomicAdd(ctr + 2, 1u);
@@ -192,10 +233,12 @@ __global__ void __launch_bounds__(kSelThreads) paged_select_kernel(const PagedAr
     });
     __syncthreads();
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
-    radix_select(sm.sel.hist, sm.sel.s, cand, need, 0u, 0u, emit);
+    radix_select(sm.sel.hist, sm.sel.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift,
+                 emit);
   } else {
     __syncthreads();
-    radix_select(sm.sel.hist, sm.sel.s, bset, need, 0u, 0u, emit);
+    radix_select(sm.sel.hist, sm.sel.s, bset, need, b1 << kCoarseShift, 32 - kCoarseShift,
+                 emit);
   }
 }
 
@@ -208,8 +251,7 @@ cudaError_t launch_score(const CUtensorMap& tv, const CUtensorMap& ts, const Pag
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)a.chunks, (unsigned)a.B);
-  kern<<<grid, kPagedThreads, smem, stream>>>(tv, ts, a);
+  kern<<<(unsigned)a.grid, kPagedThreads, smem, stream>>>(tv, ts, a);
   return cudaGetLastError();
 }
 

@@ -69,10 +69,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
   const uint32_t need = (uint32_t)k - above;
   if (fits) {
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)sm.n_cand};
-    radix_select(sm.sel.hist, sm.sel.s, cand, need, 0u, 0u, emit);
+    radix_select(sm.sel.hist, sm.sel.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift,
+                 emit);
   } else {
-    radix_select(sm.sel.hist, sm.sel.s, src, need, b1 << kCoarseShift,
-                 0xFFFFFFFFu << kCoarseShift, emit);
+    radix_select(sm.sel.hist, sm.sel.s, src, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
   }
 }
 

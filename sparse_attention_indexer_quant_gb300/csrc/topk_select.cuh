@@ -5,13 +5,10 @@
 // the top 12 key bits (sign, exponent and 3 mantissa bits: 8 bins per octave
 // at any magnitude) locates the bin holding the k-th largest value; everything
 // in higher bins is selected outright, and the exact threshold inside the
-// boundary bin is found by radix passes on the full key (11, 11 and 10 bits)
-// over the boundary elements only.  Elements equal to the final threshold key
+// boundary bin is found by radix passes over the boundary elements only, on
+// the 20 key bits below the bin (two 10-bit digits).  Elements equal to the final threshold key
 // fill the remaining slots in arrival order, so equal values may be taken in
 // any order.
-//
-// Histogram updates are aggregated per warp (one shared-memory atomic per
-// distinct bin in a warp), which keeps clustered values from serialising.
 //
 // A source visits (key, index) pairs: `src.for_each(f)` calls f(key, idx) for
 // this thread's share of the elements.  Every thread of the block must call
@@ -43,14 +40,12 @@ struct SelectScratch {
   ScanScratch s;
 };
 
-// atomicAdd(&hist[bin], 1) for every lane with pred, one atomic per distinct
-// bin in the warp.
+// atomicAdd(&hist[bin], 1) for every lane with pred.  The 12-bit bins spread
+// a warp's 32 logits over many bins, so plain shared-memory atomics see few
+// same-address conflicts; per-warp aggregation (match.any) costs more than
+// it saves here.
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool pred) {
-  const uint32_t active = __activemask();
-  const uint32_t want = __ballot_sync(active, pred);
-  if (!pred) return;
-  const uint32_t peers = __match_any_sync(want, bin);
-  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  if (pred) atomicAdd(&hist[bin], 1u);
 }
 
 // Returns a distinct slot from *counter for every lane with pred (one atomic
@@ -126,25 +121,26 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t* hist, int nbi
   __syncthreads();
 }
 
-__device__ __forceinline__ constexpr int digit_shift(int d) { return d == 0 ? 21 : d == 1 ? 10 : 0; }
-__device__ __forceinline__ constexpr uint32_t digit_mask(int d) { return d == 2 ? 0x3FFu : 0x7FFu; }
-
 // Emits (through emit(key, idx)) exactly `need` elements: the `need` largest
-// keys among those of src matching (key & mask) == prefix.  hist must hold at
-// least kRadixBins words of scratch.
+// keys among those of src whose top `known` bits equal those of `prefix`.
+// The remaining low bits are resolved in one, two or three radix digits of at
+// most 11 bits.  hist must hold at least kRadixBins words of scratch.
 template <class Src, class Emit>
 __device__ __forceinline__ void radix_select(uint32_t* hist, ScanScratch& sc, const Src& src,
-                                             uint32_t need, uint32_t prefix, uint32_t mask,
+                                             uint32_t need, uint32_t prefix, int known,
                                              Emit emit) {
-  for (int d = 0; d < 3 && need > 0; ++d) {
-    const int sh = digit_shift(d);
-    const uint32_t dm = digit_mask(d);
-    const int nb = (int)dm + 1;
+  uint32_t mask = known == 0 ? 0u : (0xFFFFFFFFu << (32 - known));
+  prefix &= mask;
+  while (known < 32 && need > 0) {
+    const int rest = 32 - known;
+    const int width = rest <= 11 ? rest : (rest <= 22 ? (rest + 1) / 2 : 11);
+    const int sh = rest - width;
+    const uint32_t dm = (1u << width) - 1u;
+    const int nb = 1 << width;
     for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     src.for_each([&](uint32_t key, int32_t) {
-      const bool m = (key & mask) == prefix;
-      hist_add(hist, (key >> sh) & dm, m);
+      hist_add(hist, (key >> sh) & dm, (key & mask) == prefix);
     });
     __syncthreads();
     find_threshold_bin(hist, nb, need, sc);
@@ -157,6 +153,7 @@ __device__ __forceinline__ void radix_select(uint32_t* hist, ScanScratch& sc, co
     need -= above;
     prefix |= b << sh;
     mask |= dm << sh;
+    known += width;
     __syncthreads();
   }
   if (need == 0) return;

@@ -87,38 +87,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Value area of the paged cache: 3-D (64 bytes, 64 rows, num_blocks) with
-// strides (64, 4352), one page per box, 64-byte swizzle.
-idx_status cache_value_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[3] = {64, 64, (cuuint64_t)num_blocks};
-  const cuuint64_t strides[2] = {64, (cuuint64_t)idx::kPageBytes};
-  const cuuint32_t box[3] = {64, 64, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(cache), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (cache values): CUresult %d", (int)r);
-  return IDX_OK;
-}
-
-// Scale area of the paged cache: 2-D (256 bytes, num_blocks), stride 4352.
-idx_status cache_scale_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[2] = {256, (cuuint64_t)num_blocks};
-  const cuuint64_t strides[1] = {(cuuint64_t)idx::kPageBytes};
-  const cuuint32_t box[2] = {256, 1};
-  const cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                  const_cast<uint8_t*>(cache + idx::kPageValBytes), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (cache scales): CUresult %d", (int)r);
-  return IDX_OK;
-}
-
 idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
                               int32_t next_n, int32_t H, const uint8_t* kcache,
                               int64_t num_blocks, int32_t page_size, const int32_t* block_table,
@@ -146,11 +114,12 @@ idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, in
 // [0, cols) are cut into items of whole 128-key tiles, about four items per
 // CTA over the batch (2..64 tiles each), and the grid holds as many CTAs as
 // fit on the device at once (or fewer when there are fewer items).
-void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh) {
+void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh, int fixed_tiles = 0) {
   const int64_t ctas = (int64_t)sms * idx::paged_ctas_per_sm(nh);
   const int64_t tiles = (cols + 127) / 128;
   int64_t per = (tiles * a.B + 4 * ctas - 1) / (4 * ctas);
   per = per < 2 ? 2 : (per > idx::kMaxTilesPerCta ? idx::kMaxTilesPerCta : per);
+  if (fixed_tiles > 0) per = fixed_tiles;
   a.tiles_per_cta = (int32_t)per;
   const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
   a.chunks = chunks > INT32_MAX ? -1 : (int32_t)chunks;
@@ -242,10 +211,8 @@ idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, 
   if (s != IDX_OK) return s;
   if (B == 0) return ok();
   if (!logits) return fail(IDX_ERR_INVALID_ARG, "null logits");
-  CUtensorMap tv, ts;
-  if ((s = cache_value_map(&tv, kcache, num_blocks)) != IDX_OK) return s;
-  if ((s = cache_scale_map(&ts, kcache, num_blocks)) != IDX_OK) return s;
   idx::PagedArgs a{};
+  a.kcache = kcache;
   a.q_vals = q_vals;
   a.q_scales = q_scales;
   a.block_table = block_table;
@@ -261,7 +228,7 @@ idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, 
   const int64_t cap = (int64_t)max_blocks * 64;
   set_paged_chunking(a, a.clean ? ld : (ld < cap ? ld : cap), sms, H * next_n);
   if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "ld too large");
-  return from_cuda(idx::launch_paged_logits(tv, ts, H, next_n, a, (cudaStream_t)stream),
+  return from_cuda(idx::launch_paged_logits(H, next_n, a, (cudaStream_t)stream),
                    "paged_mqa_logits launch");
 }
 
@@ -353,10 +320,8 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   if (workspace_bytes < need || workspace == nullptr)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
   if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
-  CUtensorMap tv, ts;
-  if ((s = cache_value_map(&tv, kcache, num_blocks)) != IDX_OK) return s;
-  if ((s = cache_scale_map(&ts, kcache, num_blocks)) != IDX_OK) return s;
   idx::PagedArgs a{};
+  a.kcache = kcache;
   a.q_vals = q_vals;
   a.q_scales = q_scales;
   a.block_table = block_table;
@@ -368,13 +333,15 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   a.B = B;
   a.max_blocks = max_blocks;
   a.clean = 0;
-  set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n);
+  int32_t item_tiles = 0;
+  idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, &item_tiles, nullptr);
+  set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n, item_tiles);
   if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks too large");
   a.topk = k;
   a.out_idx = out_idx;
   a.workspace = workspace;
   a.errors = errors;
-  return from_cuda(idx::launch_paged_logits_topk(tv, ts, H, next_n, a, (cudaStream_t)stream),
+  return from_cuda(idx::launch_paged_logits_topk(H, next_n, a, (cudaStream_t)stream),
                    "paged_logits_topk launch");
 }
 

@@ -16,9 +16,9 @@ cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_str
 cudaError_t launch_quant_q(const void* q, int64_t rows, uint8_t* vals, uint8_t* scales,
                            cudaStream_t stream);
 
-// Paged decode: tensor maps over the cache's value area (3-D: 64 B x 64 rows x
-// num_blocks, 64-byte swizzle) and scale area (2-D: 256 B x num_blocks).
+// Paged decode (persistent kernels reading the cache with cp.async).
 struct PagedArgs {
+  const uint8_t* kcache;
   const uint8_t* q_vals;
   const uint8_t* q_scales;
   const int32_t* block_table;
@@ -36,14 +36,13 @@ struct PagedArgs {
   int32_t topk;           // fused only
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only
+  uint32_t* item_counter; // zeroed work-item counter: dynamic scheduling; null: static
   idx_device_errors* errors;
 };
 
-cudaError_t launch_paged_logits(const CUtensorMap& tm_vals, const CUtensorMap& tm_scales,
-                                int H, int next_n, const PagedArgs& a, cudaStream_t stream);
+cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 
-cudaError_t launch_paged_logits_topk(const CUtensorMap& tm_vals, const CUtensorMap& tm_scales,
-                                     int H, int next_n, const PagedArgs& a, cudaStream_t stream);
+cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k,
                                   int32_t* tiles_per_cta_out, int32_t* chunks_out);
 

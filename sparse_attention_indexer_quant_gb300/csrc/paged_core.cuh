@@ -1,22 +1,26 @@
 // Persistent main loop shared by the paged decode kernels (unfused logits and
-// the scoring half of logits + top-k): each CTA loops over work items
-// (sequence b, chunk of tiles_per_item 128-key tiles) with five warp roles:
-//   warp 0      TMA producer: per tile, two 64x64-byte value boxes (64-byte
-//               swizzle) and two 256-byte scale boxes, gathered by page id,
-//               into a ring of shared-memory stages;
-//   warp 1      MMA issuer: rearranges the tile's 128 key scale words into the
-//               32x16-byte scale-factor layout, tcgen05.cp to TMEM, and two
-//               tcgen05.mma kind::mxf4 block-scaled MMAs (K = 64 each) giving
-//               D[key, j*H + h] in TMEM (fp32);
-//   warps 2-5   epilogue: one thread per key (TMEM lane) loads its row of D and
+// the scoring pass of logits + top-k): each CTA loops over work items
+// (sequence b, chunk of tiles_per_item 128-key tiles) with four warp roles:
+//   warps 0-3   epilogue: one thread per key (TMEM lane) loads its row of D and
 //               hands the next_n*H dot products to the epilogue policy `Ep`;
-//   warp 6      item loader: picks the next item (a fixed chunk-major
+//   warp 4      MMA issuer: tcgen05.cp of the tile's key scale factors to TMEM
+//               and two tcgen05.mma kind::mxf4 block-scaled MMAs (K = 64 each)
+//               giving D[key, j*H + h] in TMEM (fp32);
+//   warp 5      item loader: picks the next item (a fixed chunk-major
 //               round-robin, or a global counter when `dynamic`), stages the
 //               sequence's query heads (the MMA's B operand, N = next_n*H), their
 //               scale factors, weights and the chunk's page ids into one of two
-//               buffers, and publishes the item descriptor.
-// The stage ring, the accumulator ring and the two item buffers all run
-// across items, so the TMA stream does not drain between items.
+//               buffers, and publishes the item descriptor;
+//   warps 6-7   copy producers: per tile, the two pages' value rows (16-byte
+//               cp.async into the 64-byte-swizzled K-major layout the MMA reads)
+//               and their scale words (4-byte cp.async straight into the
+//               32x16-byte scale-factor layout), into a ring of stages.
+// Each producer thread ends a tile with cp.async.mbarrier.arrive, so the
+// stage's barrier completes when the 64 threads' copies have landed, without
+// the producers waiting on them; the MMA thread fences the generic-proxy
+// writes to the async proxy after its wait.  Page ids outside the cache are skipped (and counted) instead of
+// being read.  The stage ring, the accumulator ring and the two item buffers
+// run across items, so the copy stream does not drain between items.
 #pragma once
 
 #include "common.cuh"
@@ -24,21 +28,26 @@
 
 namespace idx {
 
-constexpr int kPagedThreads = 224;
+constexpr int kPagedThreads = 256;
 constexpr int kEpiThreads = 128;
-constexpr int kStages = 6;
+constexpr int kCopyThreads = 64;
 constexpr int kTileKeys = 128;        // MMA M: two pages
 constexpr int kTileValBytes = kTileKeys * kValBytes;  // 8192
 constexpr int kMaxTilesPerCta = 64;   // tiles per work item
+constexpr int kClCache = 1024;        // context lengths kept in shared memory
 
 __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
 }
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// CTAs per SM the persistent grid is sized for: two, except for N = 128 whose
-// epilogue needs the registers of a whole SM.
-__host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 128 ? 1 : 2; }
+// Occupancy plan per N = next_n * H.  Streaming random pages reaches HBM rate
+// only with about 200 KB of copies in flight per SM (loaded latency is several
+// microseconds), so each shape gets as many stage buffers as its CTAs-per-SM
+// allow: N = 32 three CTAs of 7 stages, N = 64 two of 10, N = 128 (whose
+// epilogue needs the registers of a whole SM) one of 20.
+__host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 32 ? 3 : nh == 64 ? 2 : 1; }
+__host__ __device__ constexpr int paged_stages(int nh) { return nh == 32 ? 7 : nh == 64 ? 10 : 20; }
 
 struct ItemDesc {
   int64_t L;        // context length after validation
@@ -51,18 +60,20 @@ struct ItemDesc {
 // Shared-memory and tensor-memory plan for N = NH query-head columns.
 template <int NH>
 struct PagedLayout {
-  static constexpr int kAccBufs = NH == 32 ? 4 : 2;
+  static constexpr int kStages = paged_stages(NH);
+  // accumulators: as many as fit the TMEM share of a CTA (512 columns per SM)
+  static constexpr int kAccBufs = NH == 32 ? 3 : 2;
   static constexpr uint32_t kSfbCol = kAccBufs * NH;        // 2 x 4 columns
   static constexpr uint32_t kSfaCol = kSfbCol + 8;          // 4 columns per accumulator
   static constexpr uint32_t kTmemCols = tmem_cols_for(kSfaCol + 4 * kAccBufs);
   static constexpr size_t kA = 0;                                      // stages x 8192 (SW64)
   static constexpr size_t kB = kA + (size_t)kStages * kTileValBytes;   // 2 x NH x 64 (SW64)
-  static constexpr size_t kSfRaw = kB + 2 * (size_t)NH * kValBytes;    // stages x 512
-  static constexpr size_t kSfa = kSfRaw + (size_t)kStages * 512;       // stages x 512
+  static constexpr size_t kSfa = kB + 2 * (size_t)NH * kValBytes;      // stages x 512
   static constexpr size_t kSfb = kSfa + (size_t)kStages * 512;         // 2 x 512
   static constexpr size_t kW = kSfb + 2 * 512;                         // 2 x NH floats
   static constexpr size_t kBt = kW + 2 * (size_t)NH * 4;               // 2 x 128 page ids
-  static constexpr size_t kItem = align_up(kBt + 2 * 2 * kMaxTilesPerCta * 4, 16);
+  static constexpr size_t kCl = kBt + 2 * 2 * kMaxTilesPerCta * 4;     // context lengths
+  static constexpr size_t kItem = align_up(kCl + kClCache * 4, 16);
   static constexpr size_t kBars = kItem + 2 * sizeof(ItemDesc);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4;
   static constexpr size_t kMisc = kBars + (size_t)kNumBars * 8;        // tmem base, abort
@@ -75,14 +86,15 @@ __host__ __device__ constexpr size_t paged_smem_bytes() {
 }
 
 // Work item w in chunk-major order: w = c * B + b.
-__device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, bool count_errors) {
+__device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, const int32_t* cl,
+                                               bool count_errors) {
   ItemDesc it;
   it.b = (int32_t)(w % p.B);
   const int64_t c = w / p.B;
   const int64_t C = (int64_t)p.tiles_per_cta * kTileKeys;
   it.k0 = c * C;
   it.k_end = it.k0 + C;
-  int64_t L = __ldg(p.context_lens + it.b);
+  int64_t L = it.b < kClCache ? cl[it.b] : __ldg(p.context_lens + it.b);
   int64_t cap = (int64_t)p.max_blocks * kPage;
   if (p.logits != nullptr && p.ld < cap) cap = p.ld;
   if (L < 0 || L > cap) {
@@ -126,23 +138,24 @@ __device__ __forceinline__ void epilogue_sync() {
 }
 
 template <int H, int NEXT_N, class Ep>
-__device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
-                                                     const CUtensorMap* tm_scales,
-                                                     const PagedArgs& p, bool dynamic,
-                                                     bool pass_empty, uint32_t* item_counter) {
+__device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const uint8_t* kcache,
+                                                     bool dynamic, bool pass_empty,
+                                                     uint32_t* item_counter) {
   constexpr int NH = H * NEXT_N;
   using Lay = PagedLayout<NH>;
   constexpr int ACC = Lay::kAccBufs;
+  constexpr int kStages = Lay::kStages;
   static_assert(NH % 32 == 0 && NH <= 128, "N must be 32, 64 or 128");
+  static_assert(Lay::kTmemCols * paged_ctas_per_sm(NH) <= 512, "TMEM over-subscribed");
 
   uint8_t* sm = aligned_smem_base();
   uint8_t* sA = sm + Lay::kA;
   uint8_t* sB = sm + Lay::kB;
-  uint8_t* sSfRaw = sm + Lay::kSfRaw;
   uint8_t* sSfa = sm + Lay::kSfa;
   uint8_t* sSfb = sm + Lay::kSfb;
   float* sW = reinterpret_cast<float*>(sm + Lay::kW);
   int32_t* sBt = reinterpret_cast<int32_t*>(sm + Lay::kBt);
+  int32_t* sCl = reinterpret_cast<int32_t*>(sm + Lay::kCl);
   ItemDesc* sItem = reinterpret_cast<ItemDesc*>(sm + Lay::kItem);
   const uint32_t bars = smem_u32(sm + Lay::kBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -158,13 +171,13 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  if (warp == 1) {
+  if (warp == 4) {
     tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), kCopyThreads);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < ACC; ++a) {
@@ -178,6 +191,8 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
     *abort = 0;
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < p.B && i < kClCache; i += kPagedThreads)
+    sCl[i] = __ldg(p.context_lens + i);
   Ep::init(extra);
   tc_fence_before();
   __syncthreads();
@@ -185,27 +200,30 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
   const uint32_t tmem = *tmem_slot;
   const int64_t n_items = (int64_t)p.B * p.chunks;
 
-  if (warp == 6) {
+  if (warp == 5) {
     // ---------------------------------------------------------- item loader
     int n = 0;
-    int64_t w = dynamic ? -1 : (int64_t)blockIdx.x - (int64_t)gridDim.x;
+    int64_t w = (int64_t)blockIdx.x - (int64_t)gridDim.x;
+    bool first = true;
     while (true) {
       ItemDesc it;
       it.n_tiles = -1;
-      // the next item with work (with pass_empty: the next item)
+      // the next item with work (with pass_empty: the next item); the first
+      // item of a CTA is its own index, later ones come from the counter
       while (true) {
-        if (dynamic) {
+        if (dynamic && !first) {
           uint32_t t = 0;
           if (lane == 0) t = atomicAdd(item_counter, 1u);
-          w = (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
+          w = (int64_t)gridDim.x + (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
         } else {
           w += gridDim.x;
         }
+        first = false;
         if (w >= n_items) {
           it.n_tiles = -1;
           break;
         }
-        it = paged_item(p, w, lane == 0);
+        it = paged_item(p, w, sCl, lane == 0);
         if (it.n_tiles > 0 || pass_empty) break;
       }
       const int qb = n & 1;
@@ -244,56 +262,70 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
       ++n;
       if (it.n_tiles < 0) break;
     }
-  } else if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------- copy producers
+    const int pt = threadIdx.x - 6 * 32;  // 0..63
     int issued = 0;
-    if (lane == 0) {
-      tma_prefetch_desc(tm_vals);
-      tma_prefetch_desc(tm_scales);
-      for (int n = 0;; ++n) {
-        const int qb = n & 1;
-        if (!mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort)) {
-          flag_timeout(p.errors, kTimeoutProducer);
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int qb = n & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort))) {
+        if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);
+        break;
+      }
+      const ItemDesc it = sItem[qb];
+      if (it.n_tiles < 0) break;
+      const int32_t* ids = sBt + qb * 2 * kMaxTilesPerCta;
+      for (int t = 0; t < it.n_tiles; ++t) {
+        const int s = issued % kStages;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ((issued / kStages) & 1) ^ 1, abort));
+        if (!ok) {
+          if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);
           break;
         }
-        const ItemDesc it = sItem[qb];
-        if (it.n_tiles < 0) break;
-        const int32_t* ids = sBt + qb * 2 * kMaxTilesPerCta;
-        bool ok = true;
-        for (int t = 0; t < it.n_tiles; ++t) {
-          const int s = issued % kStages;
-          if (!mbar_wait(empty_bar(s), ((issued / kStages) & 1) ^ 1, abort)) {
-            flag_timeout(p.errors, kTimeoutProducer);
-            ok = false;
-            break;
-          }
-          const bool two = it.k0 + (int64_t)(2 * t + 1) * kPage < it.L;
-          const int32_t id0 = ids[2 * t];
-          const int32_t id1 = ids[2 * t + 1];
-          // out-of-range ids load the TMA fill (zeros) instead of faulting
-          if (id0 < 0 || id0 >= p.num_blocks) count_bad_input(p.errors);
-          if (two && (id1 < 0 || id1 >= p.num_blocks)) count_bad_input(p.errors);
-          const uint32_t bytes = (two ? 2u : 1u) * (kPageValBytes + 256u);
-          const uint32_t fb = full_bar(s);
-          mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t a_dst = smem_u32(sA + (size_t)s * kTileValBytes);
-          const uint32_t sf_dst = smem_u32(sSfRaw + (size_t)s * 512);
-          tma_load_3d(a_dst, tm_vals, 0, 0, id0, fb);
-          tma_load_2d(sf_dst, tm_scales, 0, id0, fb);
-          if (two) {
-            tma_load_3d(a_dst + kPageValBytes, tm_vals, 0, 0, id1, fb);
-            tma_load_2d(sf_dst + 256, tm_scales, 0, id1, fb);
-          }
-          ++issued;
+        const bool two = it.k0 + (int64_t)(2 * t + 1) * kPage < it.L;
+        const int32_t id0 = ids[2 * t], id1 = ids[2 * t + 1];
+        const bool ok0 = id0 >= 0 && id0 < p.num_blocks;
+        const bool ok1 = two && id1 >= 0 && id1 < p.num_blocks;
+        if (pt == 0) {
+          if (!ok0) count_bad_input(p.errors);
+          if (two && !ok1) count_bad_input(p.errors);
         }
-        if (!ok) break;
+        const uint8_t* pg0 = kcache + (int64_t)(ok0 ? id0 : 0) * kPageBytes;
+        const uint8_t* pg1 = kcache + (int64_t)(ok1 ? id1 : 0) * kPageBytes;
+        const uint32_t a_dst = smem_u32(sA + (size_t)s * kTileValBytes);
+        // values: 512 chunks of 16 bytes; chunk q is key q/4, 16-byte column q%4
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = pt + kCopyThreads * u;
+          const int key = q >> 2, c = q & 3;
+          const bool second = key >= kPage;
+          if (second ? ok1 : ok0) {
+            const uint8_t* src = (second ? pg1 : pg0) + (key & (kPage - 1)) * kValBytes + c * 16;
+            cp_async_16(a_dst + key * kValBytes + ((c ^ ((key >> 1) & 3)) << 4), src);
+          }
+        }
+        // scales: key k's 4-byte word to 16*(k % 32) + 4*(k / 32) of the atom
+        const uint32_t sf_dst = smem_u32(sSfa + (size_t)s * 512);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int key = pt + kCopyThreads * u;
+          const bool second = key >= kPage;
+          if (second ? ok1 : ok0) {
+            const uint8_t* src =
+                (second ? pg1 : pg0) + kPageValBytes + (key & (kPage - 1)) * kScaleBytes;
+            cp_async_4(sf_dst + 16 * (key % 32) + 4 * (key / 32), src);
+          }
+        }
+        // the stage fills once all 64 threads' copies have landed; the thread
+        // holds no tile back, so its waits never depend on its own copies
+        cp_async_arrive_noinc(full_bar(s));
+        ++issued;
       }
-      // every copy this thread issued must land before the CTA can exit
-      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        if (!mbar_wait_drain(full_bar(i % kStages), (i / kStages) & 1))
-          flag_timeout(p.errors, kTimeoutDrain);
     }
-  } else if (warp == 1) {
+    // nothing may still be writing shared memory when the CTA exits
+    cp_async_wait_all();
+  } else if (warp == 4) {
     // ---------------------------------------------------------- MMA issuer
     int tiles = 0;
     bool ok = true;
@@ -322,15 +354,10 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
           break;
         }
         tc_fence_after();
-        // scale-factor atom: row l holds the 4-byte scale words of tile keys
-        // l, l+32, l+64, l+96 (key k's word is word k of the two pages' scale
-        // areas as loaded)
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(sSfRaw + (size_t)s * 512);
-        const uint4 row = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
-        *reinterpret_cast<uint4*>(sSfa + (size_t)s * 512 + 16 * lane) = row;
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
+          // the stage was written by cp.async (generic proxy); the MMA and
+          // tcgen05.cp read it through the async proxy
+          fence_proxy_async_smem();
           const uint32_t sfa_t = tmem + Lay::kSfaCol + 4u * a;
           tmem_cp_32x128b_x4(sfa_t,
                              smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
@@ -358,9 +385,9 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
       if (!mbar_wait_drain(tfull_bar(i % ACC), (i / ACC) & 1))
         flag_timeout(p.errors, kTimeoutDrain);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else {
     // ---------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int quarter = warp;  // warps 0-3: TMEM lanes [32*quarter, 32*quarter + 32)
     const int m = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     int tiles = 0;
@@ -402,7 +429,7 @@ __device__ __forceinline__ void paged_persistent_run(const CUtensorMap* tm_vals,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kTmemCols);
   }

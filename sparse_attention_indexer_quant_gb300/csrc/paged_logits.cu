@@ -5,7 +5,7 @@
 //     logit[r, s] = sum_h w[r, h] * max(0, q^[r, h] . k^[s]).
 //
 // The persistent main loop of paged_core.cuh streams each sequence's pages
-// through tcgen05 block-scaled MXF4 MMAs; this file's epilogue forms
+// (cp.async) through tcgen05 block-scaled MXF4 MMAs; this file's epilogue forms
 // sum_h w * max(0, D) for each of the next_n query rows of a key and writes it
 // to the logits row (-inf past the window when the rows are clean).
 #include <math.h>
@@ -47,7 +47,7 @@ struct UnfusedEpilogue {
     if (!p.clean) return;
     const int64_t lo = it.k0 + (int64_t)it.n_tiles * kTileKeys;
     const int64_t hi = it.k_end < p.ld ? it.k_end : p.ld;
-    const int e = threadIdx.x - 2 * 32;  // epilogue threads are warps 2-5
+    const int e = threadIdx.x;  // epilogue threads are warps 0-3
     for (int j = 0; j < NEXT_N; ++j) {
       float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
       for (int64_t s = lo + e; s < hi; s += kEpiThreads) row[s] = -INFINITY;
@@ -57,33 +57,30 @@ struct UnfusedEpilogue {
 
 template <int H, int NEXT_N>
 __global__ void __launch_bounds__(kPagedThreads, paged_ctas_per_sm(H * NEXT_N))
-    paged_logits_kernel(const __grid_constant__ CUtensorMap tm_vals,
-                        const __grid_constant__ CUtensorMap tm_scales, const PagedArgs p) {
-  paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>>(&tm_vals, &tm_scales, p, false,
-                                                              p.clean != 0, nullptr);
+    paged_logits_kernel(const PagedArgs p) {
+  paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>>(
+      p, p.kcache, p.item_counter != nullptr, p.clean != 0, p.item_counter);
 }
 
 template <int H, int NEXT_N>
-cudaError_t launch_one(const CUtensorMap& tv, const CUtensorMap& ts, const PagedArgs& a,
-                       cudaStream_t stream) {
+cudaError_t launch_one(const PagedArgs& a, cudaStream_t stream) {
   using Ep = UnfusedEpilogue<H, NEXT_N>;
   const size_t smem = paged_smem_bytes<H * NEXT_N>() + Ep::kExtraSmem;
   auto kern = paged_logits_kernel<H, NEXT_N>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)a.grid, kPagedThreads, smem, stream>>>(tv, ts, a);
+  kern<<<(unsigned)a.grid, kPagedThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_paged_logits(const CUtensorMap& tv, const CUtensorMap& ts, int H, int next_n,
-                                const PagedArgs& a, cudaStream_t stream) {
-  if (H == 32 && next_n == 1) return launch_one<32, 1>(tv, ts, a, stream);
-  if (H == 32 && next_n == 2) return launch_one<32, 2>(tv, ts, a, stream);
-  if (H == 64 && next_n == 1) return launch_one<64, 1>(tv, ts, a, stream);
-  if (H == 64 && next_n == 2) return launch_one<64, 2>(tv, ts, a, stream);
+cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
+  if (H == 32 && next_n == 1) return launch_one<32, 1>(a, stream);
+  if (H == 32 && next_n == 2) return launch_one<32, 2>(a, stream);
+  if (H == 64 && next_n == 1) return launch_one<64, 1>(a, stream);
+  if (H == 64 && next_n == 2) return launch_one<64, 2>(a, stream);
   return cudaErrorInvalidValue;
 }
 

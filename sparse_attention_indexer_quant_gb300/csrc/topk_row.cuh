@@ -1,0 +1,163 @@
+// Top-k of one logits row per CTA (vLLM API docs
+// "vllm.models.glm5next.nvidia.sparse_indexer": top_k_per_row into
+// topk_indices_buffer; rows shorter than k are padded with -1).
+//
+// The row is processed in chunks of CHUNK elements staged in shared memory:
+//   1. coarse histogram of the row (top 12 key bits: sign, exponent and three
+//      mantissa bits) while the chunk is loaded; the bin b1 holding the k-th
+//      largest value and the count above it follow from one block-wide scan;
+//   2. every thread counts its elements above b1 and in b1; one block scan of
+//      the packed counts gives each thread its output and candidate offsets, so
+//      the elements above b1 go straight to out and b1's elements to a
+//      shared-memory candidate list without atomics;
+//   3. the exact remainder among b1's elements: when they are at most the
+//      thread count, each thread ranks one of them against all the others
+//      (value, then position) and the ones ranked below the remaining count
+//      take the slots after the elements above b1; otherwise two 10-bit radix
+//      digits on the key bits below the bin.
+// A row of at most CHUNK elements is read from global memory once.  If b1
+// holds more elements than the candidate list, step 3 runs its radix passes
+// over the row itself, restricted to b1.
+#pragma once
+
+#include "common.cuh"
+#include "topk_select.cuh"
+
+namespace idx {
+
+constexpr int kRowThreads = 512;
+constexpr int kRowCandCap = 4096;
+
+template <int CHUNK>
+struct RowTopkSmem {
+  SelectScratch sel;
+  uint32_t cand_keys[kRowCandCap];
+  int32_t cand_idx[kRowCandCap];
+  uint32_t out_base;
+  uint32_t cand_base;
+  uint32_t slot;
+  uint32_t keys[CHUNK];
+};
+
+// The k largest of x[0, len) -> out[0, k) as positions 0..len-1 (any order),
+// -1 padded.  All threads of the CTA call it.
+template <int CHUNK>
+__device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __restrict__ x,
+                                         int64_t len, int32_t k, int32_t* __restrict__ out) {
+  if (len <= k) {
+    for (int64_t i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < len ? (int32_t)i : -1;
+    return;
+  }
+  const int n_chunks = (int)((len + CHUNK - 1) / CHUNK);
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sm.sel.hist[i] = 0;
+  if (threadIdx.x == 0) {
+    sm.out_base = 0;
+    sm.cand_base = 0;
+  }
+  __syncthreads();
+
+  // stage chunk c's keys in shared memory; with hist, count them too
+  auto stage = [&](int c, bool hist) {
+    const int64_t c0 = (int64_t)c * CHUNK;
+    const int n = (int)(len - c0 < CHUNK ? len - c0 : CHUNK);
+    for (int base = 0; base < n; base += kBatch * kRowThreads) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kRowThreads + threadIdx.x;
+        v[u] = i < n ? __ldcg(x + c0 + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kRowThreads + threadIdx.x;
+        if (i < n) {
+          const uint32_t key = float_key(v[u]);
+          sm.keys[i] = key;
+          if (hist) atomicAdd(&sm.sel.hist[coarse_bin(key)], 1u);
+        }
+      }
+    }
+    return n;
+  };
+
+  // ---- 1. coarse histogram
+  int n_last = 0;
+  for (int c = 0; c < n_chunks; ++c) n_last = stage(c, true);
+  __syncthreads();
+  find_threshold_bin(sm.sel.hist, kCoarseBins, (uint32_t)k, sm.sel.s);
+  const uint32_t b1 = sm.sel.s.bin;
+  const uint32_t above = sm.sel.s.above;
+  const uint32_t nb1 = sm.sel.hist[b1];
+  const bool fits = nb1 <= (uint32_t)kRowCandCap;
+
+  // ---- 2. elements above b1 to out, b1's elements to the candidate list
+  for (int c = 0; c < n_chunks; ++c) {
+    int n = n_last;
+    if (n_chunks > 1) {
+      __syncthreads();
+      n = stage(c, false);
+      __syncthreads();
+    }
+    // thread t takes elements t, t + 512, ... (conflict-free shared reads);
+    // its outputs go to a range of its own
+    uint32_t n_gt = 0, n_eq = 0;
+    for (int i = threadIdx.x; i < n; i += kRowThreads) {
+      const uint32_t bin = coarse_bin(sm.keys[i]);
+      n_gt += bin > b1 ? 1u : 0u;
+      n_eq += bin == b1 ? 1u : 0u;
+    }
+    // both block sums fit 16 bits: fewer than k <= 2048 elements of the row
+    // lie above b1, and a chunk holds at most 32768 elements of b1
+    const uint32_t packed = (n_gt << 16) | n_eq;
+    const uint32_t excl = block_exclusive_scan(packed, sm.sel.s);
+    uint32_t o = sm.out_base + (excl >> 16);
+    uint32_t cc = sm.cand_base + (excl & 0xFFFFu);
+    const int64_t c0 = (int64_t)c * CHUNK;
+    for (int i = threadIdx.x; i < n; i += kRowThreads) {
+      const uint32_t key = sm.keys[i];
+      const uint32_t bin = coarse_bin(key);
+      if (bin > b1) out[o++] = (int32_t)(c0 + i);
+      if (bin == b1) {
+        if (fits) {
+          sm.cand_keys[cc] = key;
+          sm.cand_idx[cc] = (int32_t)(c0 + i);
+        }
+        ++cc;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      sm.out_base = o;  // the last thread's offsets are the running totals
+      sm.cand_base = cc;
+    }
+    __syncthreads();
+  }
+
+  // ---- 3. the exact remainder inside b1
+  const uint32_t need = (uint32_t)k - above;
+  if (nb1 <= (uint32_t)kRowThreads) {
+    if (threadIdx.x < nb1) {
+      const uint32_t key = sm.cand_keys[threadIdx.x];
+      const int32_t pos = sm.cand_idx[threadIdx.x];
+      uint32_t rank = 0;
+      for (uint32_t q = 0; q < nb1; ++q) {
+        const uint32_t kq = sm.cand_keys[q];
+        rank += (kq > key || (kq == key && sm.cand_idx[q] < pos)) ? 1u : 0u;
+      }
+      if (rank < need) out[above + rank] = pos;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) sm.slot = above;
+  __syncthreads();
+  auto emit = [&](uint32_t, int32_t i) { out[warp_claim(&sm.slot, true)] = i; };
+  if (fits) {
+    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
+    radix_select(sm.sel.hist, sm.sel.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+  } else {
+    const GlobalLogits<true> row{x, 0, len};
+    radix_select(sm.sel.hist, sm.sel.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+  }
+}
+
+}  // namespace idx

@@ -41,7 +41,7 @@ TOPK = 2048
 L2_FLUSH_BYTES = 256 << 20   # 2x the 129 MB L2
 # sources of the fused decode entry (scoring + select launches); the committed
 # traffic figure is only used while their digest matches
-FUSED_SOURCES = ["paged_topk.cu", "paged_logits.cu", "paged_core.cuh", "topk_row.cuh",
+FUSED_SOURCES = ["paged_topk.cu", "paged_logits.cu", "paged_core.cuh",
                  "topk_select.cuh", "common.cuh"]
 
 
@@ -237,14 +237,14 @@ def run_ours(args, rank, world, local_rank):
     qs = torch.empty((p.rows * p.H, 4), dtype=torch.uint8, device=dev)
     out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
 
     def flush_l2():
         # write a buffer twice the size of L2, then read it back: afterwards no
         # input of the step is resident and no dirty line is left for the
         # timed kernels to write back
         flush.fill_(1)
-        torch.sum(flush, dtype=torch.int64, out=flush_sink)
+        torch.sum(flush, 0, dtype=torch.int64, out=flush_sink)
 
     stream = torch.cuda.current_stream()
 

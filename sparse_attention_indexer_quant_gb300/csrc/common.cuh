@@ -141,6 +141,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Kernels launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running.  pdl_wait() blocks until that
+// kernel has completed and its writes are visible (a no-op for a normal
+// launch); nothing written by earlier work may be read before it.
+// pdl_launch_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 
 // 16 bytes global -> shared, through L2 only.

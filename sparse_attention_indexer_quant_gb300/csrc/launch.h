@@ -37,10 +37,30 @@ struct PagedArgs {
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only
   uint32_t* item_counter; // zeroed work-item counter: dynamic scheduling; null: static
+  uint32_t* row_hist;     // zeroed [rows][4096] coarse histograms of the valid logits, or null
   idx_device_errors* errors;
 };
 
 cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
+
+// Launches kern<<<grid, block, smem, stream>>>(args...) with programmatic stream
+// serialization: the kernel may be scheduled while the previous kernel in the
+// stream is finishing, and must call pdl_wait() before reading its inputs.
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k,

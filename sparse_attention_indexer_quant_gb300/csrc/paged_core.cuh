@@ -191,6 +191,11 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     *abort = 0;
     fence_mbar_init();
   }
+  // up to here only this CTA's shared and tensor memory was touched: with a
+  // dependent launch that overlaps the previous kernel's tail; every input is
+  // read after the wait
+  pdl_launch_dependents();
+  pdl_wait();
   for (int i = threadIdx.x; i < p.B && i < kClCache; i += kPagedThreads)
     sCl[i] = __ldg(p.context_lens + i);
   Ep::init(extra);

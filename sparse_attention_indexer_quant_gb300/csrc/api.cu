@@ -120,6 +120,7 @@ void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh, int fi
   int64_t per = (tiles * a.B + 4 * ctas - 1) / (4 * ctas);
   per = per < 2 ? 2 : (per > idx::kMaxTilesPerCta ? idx::kMaxTilesPerCta : per);
   if (fixed_tiles > 0) per = fixed_tiles;
+  a.sms = sms;
   a.tiles_per_cta = (int32_t)per;
   const int64_t chunks = (cols + per * 128 - 1) / (per * 128);
   a.chunks = chunks > INT32_MAX ? -1 : (int32_t)chunks;
@@ -294,7 +295,7 @@ idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const in
 size_t idx_paged_logits_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks,
                                              int32_t page_size, int32_t k) {
   (void)page_size;
-  return idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, nullptr, nullptr);
+  return idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k);
 }
 
 idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
@@ -316,7 +317,7 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
     return fail(IDX_ERR_INVALID_ARG, "B*next_n=%d above 65535", B * next_n);
   int sms = 0;
   if ((s = current_device_ok(&sms)) != IDX_OK) return s;
-  const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, nullptr, nullptr);
+  const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k);
   if (workspace_bytes < need || workspace == nullptr)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
   if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
@@ -333,8 +334,8 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   a.B = B;
   a.max_blocks = max_blocks;
   a.clean = 0;
-  int32_t item_tiles = 0;
-  idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k, &item_tiles, nullptr);
+  const int32_t item_tiles = idx::paged_topk_item_tiles(
+      B, max_blocks, (int64_t)sms * idx::paged_ctas_per_sm(H * next_n));
   set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n, item_tiles);
   if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks too large");
   a.topk = k;

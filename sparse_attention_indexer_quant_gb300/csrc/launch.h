@@ -33,6 +33,7 @@ struct PagedArgs {
   int32_t tiles_per_cta;  // keys per work item = 128 * tiles_per_cta
   int32_t chunks;         // work items per sequence
   int32_t grid;           // persistent CTAs
+  int32_t sms;            // SMs of the device
   int32_t topk;           // fused only
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only
@@ -62,9 +63,31 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// launch_dependent with thread-block clusters of cluster_x CTAs along x.
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
-size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k,
-                                  int32_t* tiles_per_cta_out, int32_t* chunks_out);
+size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k);
+// 128-key tiles per work item of the fused scoring pass
+int32_t paged_topk_item_tiles(int32_t B, int32_t max_blocks, int64_t ctas);
 
 // Prefill: tensor maps over contiguous keys (values 2-D: 64 B x S, 64-byte
 // swizzle; scales 2-D: 512 B x ceil(S/128) tiles).

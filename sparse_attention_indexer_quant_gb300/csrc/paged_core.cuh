@@ -85,6 +85,17 @@ __host__ __device__ constexpr size_t paged_smem_bytes() {
   return PagedLayout<NH>::kExtra + 1024;  // + slack to align the base to 1024
 }
 
+// Keys of a sequence the kernels read: its context length clamped to the
+// block table (and to the logits row when there is one).
+__device__ __forceinline__ int64_t len_cap(const PagedArgs& p) {
+  int64_t cap = (int64_t)p.max_blocks * kPage;
+  if (p.logits != nullptr && p.ld < cap) cap = p.ld;
+  return cap;
+}
+__device__ __forceinline__ int64_t clamp_len(int64_t L, int64_t cap) {
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
 // Work item w in chunk-major order: w = c * B + b.
 __device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, const int32_t* cl,
                                                bool count_errors) {
@@ -95,8 +106,7 @@ __device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, co
   it.k0 = c * C;
   it.k_end = it.k0 + C;
   int64_t L = it.b < kClCache ? cl[it.b] : __ldg(p.context_lens + it.b);
-  int64_t cap = (int64_t)p.max_blocks * kPage;
-  if (p.logits != nullptr && p.ld < cap) cap = p.ld;
+  const int64_t cap = len_cap(p);
   if (L < 0 || L > cap) {
     if (count_errors && c == 0) count_bad_input(p.errors);
     L = L < 0 ? 0 : cap;
@@ -207,6 +217,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
 
   if (warp == 5) {
     // ---------------------------------------------------------- item loader
+    constexpr uint32_t kAll = 0xFFFFFFFFu;
     int n = 0;
     int64_t w = (int64_t)blockIdx.x - (int64_t)gridDim.x;
     bool first = true;
@@ -219,7 +230,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
         if (dynamic && !first) {
           uint32_t t = 0;
           if (lane == 0) t = atomicAdd(item_counter, 1u);
-          w = (int64_t)gridDim.x + (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
+          w = (int64_t)gridDim.x + (int64_t)__shfl_sync(kAll, t, 0);
         } else {
           w += gridDim.x;
         }
@@ -231,34 +242,60 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
         it = paged_item(p, w, sCl, lane == 0);
         if (it.n_tiles > 0 || pass_empty) break;
       }
+      // the item's operands are read into registers before waiting for its
+      // buffer, all loads of a lane in flight together:
+      //   B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
+      //   stored with the 64-byte swizzle (16-byte chunk c of row r at chunk
+      //   c ^ ((r >> 1) & 3)); its scale factors in the 32x16-byte atom (row
+      //   r's 4 bytes at 16*(r % 32) + 4*(r / 32), rows past NH zero); the
+      //   weights; the item's page ids.
+      constexpr int kQv = NH * 4 / 32;
+      uint4 qv_r[kQv];
+      uint32_t sf_r[4];
+      float w_r[NH / 32];
+      int32_t id_r[4];
+      if (it.n_tiles > 0) {
+        const uint4* qv = reinterpret_cast<const uint4*>(p.q_vals + (int64_t)it.b * NH * kValBytes);
+#pragma unroll
+        for (int u = 0; u < kQv; ++u) qv_r[u] = __ldg(qv + lane + 32 * u);
+        const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)it.b * NH;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sf_r[u] = lane + 32 * u < NH ? __ldg(qs + lane + 32 * u) : 0u;
+#pragma unroll
+        for (int u = 0; u < NH / 32; ++u) w_r[u] = __ldg(p.weights + (int64_t)it.b * NH + lane + 32 * u);
+        // page ids of the item's tiles (the entries past the sequence's last
+        // page are never used: the producers skip those pages)
+        const int32_t* bt = p.block_table + (int64_t)it.b * p.max_blocks + it.k0 / kPage;
+        const int64_t in_row = (int64_t)p.max_blocks - it.k0 / kPage;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = lane + 32 * u;
+          id_r[u] = i < 2 * it.n_tiles && i < in_row ? __ldg(bt + i) : 0;
+        }
+      }
       const int qb = n & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(qempty_bar(qb), ((n >> 1) & 1) ^ 1, abort))) {
+      if (!__all_sync(kAll, mbar_wait(qempty_bar(qb), ((n >> 1) & 1) ^ 1, abort))) {
         if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);
         break;
       }
       if (it.n_tiles > 0) {
-        // B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
-        // stored with the 64-byte swizzle (16-byte chunk c of row r at chunk
-        // c ^ ((r >> 1) & 3)); its scale factors in the 32x16-byte atom (row
-        // r's 4 bytes at 16*(r % 32) + 4*(r / 32), rows past NH zero).
         uint8_t* b_dst = sB + (size_t)qb * NH * kValBytes;
-        const uint8_t* qv = p.q_vals + (int64_t)it.b * NH * kValBytes;
-        for (int i = lane; i < NH * 4; i += 32) {
+#pragma unroll
+        for (int u = 0; u < kQv; ++u) {
+          const int i = lane + 32 * u;
           const int r = i >> 2, ch = i & 3;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qv + r * kValBytes) + ch);
-          *reinterpret_cast<uint4*>(b_dst + r * kValBytes + ((ch ^ ((r >> 1) & 3)) << 4)) = v;
+          *reinterpret_cast<uint4*>(b_dst + r * kValBytes + ((ch ^ ((r >> 1) & 3)) << 4)) = qv_r[u];
         }
-        const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)it.b * NH;
-        for (int r = lane; r < 128; r += 32) {
-          const uint32_t wv = r < NH ? __ldg(qs + r) : 0u;
-          *reinterpret_cast<uint32_t*>(sSfb + qb * 512 + 16 * (r % 32) + 4 * (r / 32)) = wv;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)  // row lane + 32u
+          *reinterpret_cast<uint32_t*>(sSfb + qb * 512 + 16 * lane + 4 * u) = sf_r[u];
+#pragma unroll
+        for (int u = 0; u < NH / 32; ++u) sW[qb * NH + lane + 32 * u] = w_r[u];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = lane + 32 * u;
+          if (i < 2 * it.n_tiles) sBt[qb * 2 * kMaxTilesPerCta + i] = id_r[u];
         }
-        for (int r = lane; r < NH; r += 32)
-          sW[qb * NH + r] = __ldg(p.weights + (int64_t)it.b * NH + r);
-        const int32_t* bt = p.block_table + (int64_t)it.b * p.max_blocks + it.k0 / kPage;
-        const int n_pages = (int)((it.L - it.k0 + kPage - 1) / kPage);
-        for (int i = lane; i < 2 * it.n_tiles; i += 32)
-          sBt[qb * 2 * kMaxTilesPerCta + i] = i < n_pages ? __ldg(bt + i) : 0;
       }
       if (lane == 0) sItem[qb] = it;
       fence_proxy_async_smem();
@@ -270,6 +307,9 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   } else if (warp >= 6) {
     // ---------------------------------------------------------- copy producers
     const int pt = threadIdx.x - 6 * 32;  // 0..63
+    // the cache is streamed once per call: its lines go first, so that the
+    // logits written meanwhile stay in L2 for whatever reads them next
+    const uint64_t pol = l2_evict_first_policy();
     int issued = 0;
     bool ok = true;
     for (int n = 0; ok; ++n) {
@@ -307,7 +347,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
           const bool second = key >= kPage;
           if (second ? ok1 : ok0) {
             const uint8_t* src = (second ? pg1 : pg0) + (key & (kPage - 1)) * kValBytes + c * 16;
-            cp_async_16(a_dst + key * kValBytes + ((c ^ ((key >> 1) & 3)) << 4), src);
+            cp_async_16(a_dst + key * kValBytes + ((c ^ ((key >> 1) & 3)) << 4), src, pol);
           }
         }
         // scales: key k's 4-byte word to 16*(k % 32) + 4*(k / 32) of the atom
@@ -319,7 +359,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
           if (second ? ok1 : ok0) {
             const uint8_t* src =
                 (second ? pg1 : pg0) + kPageValBytes + (key & (kPage - 1)) * kScaleBytes;
-            cp_async_4(sf_dst + 16 * (key % 32) + 4 * (key / 32), src);
+            cp_async_4(sf_dst + 16 * (key % 32) + 4 * (key / 32), src, pol);
           }
         }
         // the stage fills once all 64 threads' copies have landed; the thread

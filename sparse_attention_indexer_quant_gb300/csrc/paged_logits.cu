@@ -77,6 +77,9 @@ cudaError_t launch_one(const PagedArgs& a, cudaStream_t stream) {
   auto kern = paged_logits_kernel<H, NEXT_N>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3((unsigned)a.grid), dim3(kPagedThreads), smem, stream, a);
 }

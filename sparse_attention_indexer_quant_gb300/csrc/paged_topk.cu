@@ -1,25 +1,29 @@
 // Paged decode logits + top-k (vLLM API docs "vllm.models.glm5next.nvidia.sparse_indexer":
-// paged_mqa_logits followed by top_k_per_row into topk_indices_buffer), in two
+// paged_mqa_logits followed by top_k_per_row into topk_indices_buffer), in
 // launches that hand the logits over through the caller's workspace instead of
 // a logits tensor:
 //
-//   1. score    the persistent cp.async + tcgen05 logits kernel, taking work items
-//               from a counter in the workspace, writing each row's valid
-//               logits to a row-major scratch that stays in L2 for these sizes
-//               and counting each logit into its row's coarse histogram (the
-//               top 12 bits of its order-preserving key);
-//   2. select   one 1024-thread CTA per row: the row's histogram gives the bin
-//               holding the k-th largest logit and the count above it; one pass
-//               over the row's logits sends everything above that bin to the
-//               output and the bin's own elements to a shared-memory candidate
-//               list; two 10-bit radix digits over the candidates finish the
-//               exact selection.
-// All three launches (zeroing, score, select) are dependent launches, so each
-// one's start overlaps the previous one's tail.
+//   1. zero     the work-item counter and the row histograms;
+//   2. score    the persistent cp.async + tcgen05 logits kernel, taking work items
+//               from the counter, writing each row's valid logits to a
+//               row-major scratch that stays in L2 for these sizes and counting
+//               each logit into its row's coarse histogram (the top 12 bits of
+//               its order-preserving key);
+//   3. select   one thread-block cluster of P CTAs per row, each CTA over a
+//               slice of the row: the row's histogram gives the bin b1 holding
+//               the k-th largest logit and the count above it; each thread
+//               counts its elements above and in b1, one block scan and one
+//               exchange of CTA totals through distributed shared memory give
+//               every thread its output and candidate slots; the elements above
+//               b1 go straight to the output and b1's elements into the
+//               cluster leader's shared memory, where two 10-bit radix digits
+//               finish the exact selection.
+// All three are dependent launches, so each one's start overlaps the previous
+// one's tail.
 //
-// Workspace (device, caller-owned): a u32 work-item counter and the u32
-// histograms [rows][4096] (both zeroed by a small kernel per call), then f32
-// logits[rows][ldw], ldw = max_blocks * 64.
+// Workspace (device, caller-owned), 256-byte aligned pieces: the u32 work-item
+// counter and u32 histograms [rows][4096] (both zeroed per call), then f32
+// logits [rows][ldw], ldw = max_blocks * 64.
 #include <math.h>
 
 #include "common.cuh"
@@ -30,11 +34,13 @@
 namespace idx {
 namespace {
 
-constexpr int kFusedTilesPerItem = 8;
-constexpr int kSelThreads = 1024;
-constexpr int kSelCandCap = 8192;  // boundary-bin elements kept in shared memory
-constexpr int kSelVec = 4;         // float4 loads in flight per thread in the row pass
-static_assert(kCoarseBins == 4 * kSelThreads, "each select thread owns four histogram bins");
+constexpr int kSelThreads = 512;
+constexpr int kSelVec = 4;                              // float4 loads per thread per chunk
+constexpr int kSelChunk = kSelThreads * 4 * kSelVec;    // 8192 elements
+constexpr int kCandSmem = 8192;                         // boundary-bin elements in the leader
+constexpr int kMaxParts = 8;                            // portable cluster size
+constexpr int kMinSlice = 4096;                         // elements per CTA at least
+static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
 
 struct TopkWs {
   uint32_t* items;    // work-item counter of the scoring pass
@@ -49,38 +55,120 @@ __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 
 __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t max_blocks,
                                             size_t* total) {
   const int64_t ldw = (int64_t)max_blocks * kPage;
-  const size_t c = 256;
-  const size_t h = (size_t)rows * kCoarseBins * 4;
-  const size_t e = ws_align((size_t)rows * ldw * 4);
+  const size_t o_hist = 256;
+  const size_t o_lg = o_hist + (size_t)rows * kCoarseBins * 4;
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
   w.items = reinterpret_cast<uint32_t*>(p);
-  w.hist = reinterpret_cast<uint32_t*>(p + c);
-  w.logits = reinterpret_cast<float*>(p + c + h);
+  w.hist = reinterpret_cast<uint32_t*>(p + o_hist);
+  w.logits = reinterpret_cast<float*>(p + o_lg);
   w.ldw = ldw;
-  w.zero_bytes = c + h;
-  if (total) *total = c + h + e;
+  w.zero_bytes = o_lg;
+  if (total) *total = o_lg + ws_align((size_t)rows * ldw * 4);
   return w;
 }
 
 struct SelSmem {
-  uint32_t hist[kRadixBins];  // radix-digit scratch
+  uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
-  uint32_t n_out;             // elements above the boundary bin placed so far
-  uint32_t n_cand;            // boundary-bin elements seen so far
-  uint32_t slot;              // next output slot of the exact pass
-  uint32_t cand_keys[kSelCandCap];
-  int32_t cand_idx[kSelCandCap];
+  uint32_t warp_gt[kSelThreads / 32], warp_eq[kSelThreads / 32];
+  uint32_t cta_gt, cta_eq;     // this CTA's counts above / in b1 (read by the cluster)
+  uint32_t o_base, c_base;     // this CTA's first output / candidate slot
+  uint32_t all_eq;             // the row's elements in b1
+  uint32_t slot;               // next output slot of the exact pass
+  uint32_t cand_keys[kCandSmem];
+  int32_t cand_idx[kCandSmem];
 };
 
-__global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const PagedArgs p,
-                                                                       int next_n) {
+// Thread t's 8 histogram bins, highest first: 4095 - 8t down to 4088 - 8t.
+__device__ __forceinline__ void load_bins(const uint32_t* hist, int t, uint32_t (&hb)[8]) {
+  const uint4* h = reinterpret_cast<const uint4*>(hist) + 2 * (kSelThreads - 1 - t);
+  const uint4 lo = __ldcg(h), hi = __ldcg(h + 1);  // bins base..base+3, base+4..base+7
+  hb[0] = hi.w; hb[1] = hi.z; hb[2] = hi.y; hb[3] = hi.x;
+  hb[4] = lo.w; hb[5] = lo.z; hb[6] = lo.y; hb[7] = lo.x;
+}
+
+// Keys of x[i] for this thread's 16 positions of the chunk at `base`
+// (key(-inf) outside [base, s1): its bin lies below the bin of any finite
+// logit, so such positions are neither counted nor taken).
+__device__ __forceinline__ void load_chunk_keys(const float* x, int64_t base, int64_t s1, int t,
+                                                uint4 (&kv)[kSelVec]) {
+#pragma unroll
+  for (int u = 0; u < kSelVec; ++u) {
+    const int64_t i0 = base + 4 * ((int64_t)u * kSelThreads + t);
+    float4 v;
+    if (i0 + 3 < s1) {
+      v = __ldca(reinterpret_cast<const float4*>(x + i0));
+    } else {
+      v.x = i0 + 0 < s1 ? __ldca(x + i0 + 0) : -INFINITY;
+      v.y = i0 + 1 < s1 ? __ldca(x + i0 + 1) : -INFINITY;
+      v.z = i0 + 2 < s1 ? __ldca(x + i0 + 2) : -INFINITY;
+      v.w = i0 + 3 < s1 ? __ldca(x + i0 + 3) : -INFINITY;
+    }
+    kv[u] = make_uint4(float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w));
+  }
+}
+
+__device__ __forceinline__ void count_keys(const uint4 (&kv)[kSelVec], uint32_t b1, uint32_t& n_gt,
+                                           uint32_t& n_eq) {
+#pragma unroll
+  for (int u = 0; u < kSelVec; ++u) {
+    const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t bin = coarse_bin(e4[q]);
+      n_gt += bin > b1 ? 1u : 0u;
+      n_eq += bin == b1 ? 1u : 0u;
+    }
+  }
+}
+
+// Exclusive prefix sums of a and b over the block's threads (ea, eb) and their
+// block totals (ta, tb).  The caller syncs before the scratch is reused.
+__device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b, uint32_t& ea,
+                                            uint32_t& eb, uint32_t& ta, uint32_t& tb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t xa = a, xb = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t ya = __shfl_up_sync(0xFFFFFFFFu, xa, o);
+    const uint32_t yb = __shfl_up_sync(0xFFFFFFFFu, xb, o);
+    if (lane >= o) {
+      xa += ya;
+      xb += yb;
+    }
+  }
+  if (lane == 31) {
+    sm.warp_gt[warp] = xa;
+    sm.warp_eq[warp] = xb;
+  }
+  __syncthreads();
+  uint32_t pa = 0, pb = 0, sa = 0, sb = 0;
+#pragma unroll
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    const uint32_t va = sm.warp_gt[w], vb = sm.warp_eq[w];
+    pa += w < warp ? va : 0u;
+    pb += w < warp ? vb : 0u;
+    sa += va;
+    sb += vb;
+  }
+  ea = pa + xa - a;
+  eb = pb + xb - b;
+  ta = sa;
+  tb = sb;
+}
+
+// Launched as clusters of `parts` CTAs, one cluster per row.  Every CTA of a
+// cluster takes the same branches and passes the same two cluster barriers.
+__global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const PagedArgs p, int next_n,
+                                                                      int parts) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   pdl_wait();  // the scoring pass's logits and histograms
   const int64_t rows = (int64_t)p.B * next_n;
   const TopkWs ws = ws_layout(p.workspace, rows, p.max_blocks, nullptr);
-  const int64_t r = blockIdx.x;
+  const int64_t r = blockIdx.x / parts;
+  const int part = (int)cluster_ctarank();
   const int b = (int)(r / next_n), j = (int)(r % next_n);
   int64_t L = __ldg(p.context_lens + b);
   const int64_t cap = (int64_t)p.max_blocks * kPage;
@@ -90,79 +178,93 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   const uint32_t k = (uint32_t)p.topk;
   int32_t* out = p.out_idx + r * p.topk;
   const int t = threadIdx.x;
-  if (len <= (int64_t)k) {
-    for (int i = t; i < (int)k; i += kSelThreads) out[i] = i < len ? i : -1;
+  if (len <= (int64_t)k) {  // the whole cluster leaves here
+    if (part == 0)
+      for (int i = t; i < (int)k; i += kSelThreads) out[i] = i < len ? i : -1;
     return;
   }
+  const int64_t slice = ((len + parts - 1) / parts + 3) / 4 * 4;
+  const int64_t s0 = (int64_t)part * slice;
+  const int64_t s1 = s0 + slice < len ? s0 + slice : len;
+  const int n_chunks = (int)((slice + kSelChunk - 1) / kSelChunk);
+  const float* x = ws.logits + r * ws.ldw;  // 256-byte aligned; slices 16-byte aligned
 
-  // ---- 1. boundary bin from the row's histogram; thread t owns bins
-  //         4095-4t down to 4092-4t, so thread order is descending bin order
-  const uint4 h4 = __ldcg(reinterpret_cast<const uint4*>(ws.hist + r * kCoarseBins) +
-                          (kSelThreads - 1 - t));
-  if (t == 0) {
-    sm.s.bin = 0;
-    sm.s.above = 0;
-    sm.n_out = 0;
-    sm.n_cand = 0;
-  }
-  const uint32_t local = h4.x + h4.y + h4.z + h4.w;
-  const uint32_t excl = block_exclusive_scan(local, sm.s);
-  if (excl < k && k <= excl + local) {
-    const uint32_t hb[4] = {h4.w, h4.z, h4.y, h4.x};
-    uint32_t run = excl;
+  // the first two chunks' loads go out together with the histogram's
+  uint4 ka[kSelVec], kb[kSelVec];
+  load_chunk_keys(x, s0, s1, t, ka);
+  load_chunk_keys(x, s0 + kSelChunk, s1, t, kb);
+
+  // ---- 1. boundary bin from the row's histogram (every CTA of the row)
+  uint32_t b1, above;
+  {
+    uint32_t hb[8];
+    load_bins(ws.hist + r * kCoarseBins, t, hb);
+    if (t == 0) {
+      sm.s.bin = 0;
+      sm.s.above = 0;
+    }
+    uint32_t local = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (run < k && k <= run + hb[q]) {
-        sm.s.bin = (uint32_t)(kCoarseBins - 1 - 4 * t - q);
-        sm.s.above = run;
+    for (int q = 0; q < 8; ++q) local += hb[q];
+    const uint32_t excl = block_exclusive_scan(local, sm.s);
+    if (excl < k && k <= excl + local) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run < k && k <= run + hb[q]) {
+          sm.s.bin = (uint32_t)(kCoarseBins - 1 - 8 * t - q);
+          sm.s.above = run;
+        }
+        run += hb[q];
       }
-      run += hb[q];
+    }
+    __syncthreads();
+    b1 = sm.s.bin;
+    above = sm.s.above;
+  }
+
+  // ---- 2a. this thread's counts above b1 and in b1 over the slice
+  uint32_t n_gt = 0, n_eq = 0;
+  count_keys(ka, b1, n_gt, n_eq);
+  count_keys(kb, b1, n_gt, n_eq);
+  for (int c = 2; c < n_chunks; c += 2) {  // (then 2c reloads every chunk)
+    load_chunk_keys(x, s0 + (int64_t)c * kSelChunk, s1, t, ka);
+    load_chunk_keys(x, s0 + (int64_t)(c + 1) * kSelChunk, s1, t, kb);
+    count_keys(ka, b1, n_gt, n_eq);
+    count_keys(kb, b1, n_gt, n_eq);
+  }
+
+  // ---- 2b. slots: block scan, then the CTAs of the row trade totals
+  uint32_t eg, ee, tg, te;
+  block_scan2(sm, n_gt, n_eq, eg, ee, tg, te);
+  if (t == 0) {
+    sm.cta_gt = tg;
+    sm.cta_eq = te;
+  }
+  cluster_sync_all();  // every CTA's totals are visible
+  if (t < 32) {  // lane q reads CTA q's totals, all in flight together
+    uint32_t g = 0, e = 0;
+    if (t < parts) {
+      g = ld_cluster_u32(cluster_map(smem_u32(&sm.cta_gt), t));
+      e = ld_cluster_u32(cluster_map(smem_u32(&sm.cta_eq), t));
+    }
+    const uint32_t bg = __reduce_add_sync(0xFFFFFFFFu, t < part ? g : 0u);
+    const uint32_t be = __reduce_add_sync(0xFFFFFFFFu, t < part ? e : 0u);
+    const uint32_t ae = __reduce_add_sync(0xFFFFFFFFu, e);
+    if (t == 0) {
+      sm.o_base = bg;
+      sm.c_base = be;
+      sm.all_eq = ae;
     }
   }
   __syncthreads();
-  const uint32_t b1 = sm.s.bin;
-  const uint32_t above = sm.s.above;
 
-  // ---- 2. one pass over the row: above b1 -> out, b1 -> candidates.  Per
-  //         chunk of 16K elements each thread holds its 16 keys in registers,
-  //         counts them, and one block scan of the packed counts gives every
-  //         thread its own output and candidate ranges (no atomics).
-  const float* x = ws.logits + r * ws.ldw;  // 256-byte aligned
-  constexpr int64_t kPass = (int64_t)kSelThreads * 4 * kSelVec;
-  for (int64_t base = 0; base < len; base += kPass) {
-    uint4 kv[kSelVec];
-#pragma unroll
-    for (int u = 0; u < kSelVec; ++u) {
-      const int64_t i0 = base + 4 * ((int64_t)u * kSelThreads + t);
-      float4 v;
-      if (i0 + 3 < len) {
-        v = __ldcg(reinterpret_cast<const float4*>(x + i0));
-      } else {
-        v.x = i0 + 0 < len ? __ldcg(x + i0 + 0) : -INFINITY;
-        v.y = i0 + 1 < len ? __ldcg(x + i0 + 1) : -INFINITY;
-        v.z = i0 + 2 < len ? __ldcg(x + i0 + 2) : -INFINITY;
-        v.w = i0 + 3 < len ? __ldcg(x + i0 + 3) : -INFINITY;
-      }
-      kv[u] = make_uint4(float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w));
-    }
-    // positions past len hold key(-inf), whose bin (0x007) lies below any bin
-    // that can hold the k-th largest of at least k + 1 finite logits
-    uint32_t n_gt = 0, n_eq = 0;
-#pragma unroll
-    for (int u = 0; u < kSelVec; ++u) {
-      const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t bin = coarse_bin(e4[q]);
-        n_gt += bin > b1 ? 1u : 0u;
-        n_eq += bin == b1 ? 1u : 0u;
-      }
-    }
-    // block sums fit 16 bits: fewer than k <= 2048 elements lie above b1 and a
-    // chunk holds 16384 elements
-    const uint32_t ex = block_exclusive_scan((n_gt << 16) | n_eq, sm.s);
-    uint32_t o = sm.n_out + (ex >> 16);
-    uint32_t c = sm.n_cand + (ex & 0xFFFFu);
+  // ---- 2c. elements above b1 -> out, b1's elements -> the leader's list
+  const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
+  const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
+  uint32_t o = sm.o_base + eg;
+  uint32_t ce = sm.c_base + ee;
+  auto scatter = [&](const uint4 (&kv)[kSelVec], int64_t base) {
 #pragma unroll
     for (int u = 0; u < kSelVec; ++u) {
       const int64_t i0 = base + 4 * ((int64_t)u * kSelThreads + t);
@@ -174,35 +276,43 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
           if (o < above) out[o] = (int32_t)(i0 + q);
           ++o;
         } else if (bin == b1) {
-          if (c < (uint32_t)kSelCandCap) {
-            sm.cand_keys[c] = e4[q];
-            sm.cand_idx[c] = (int32_t)(i0 + q);
+          if (ce < (uint32_t)kCandSmem) {
+            st_cluster_u32(cand_keys0 + 4u * ce, e4[q]);
+            st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)(i0 + q));
           }
-          ++c;
+          ++ce;
         }
       }
     }
-    __syncthreads();
-    if (t == kSelThreads - 1) {  // the last thread's ends are the running totals
-      sm.n_out = o;
-      sm.n_cand = c;
+  };
+  if (n_chunks <= 2) {  // still in registers
+    scatter(ka, s0);
+    scatter(kb, s0 + kSelChunk);
+  } else {
+    for (int c = 0; c < n_chunks; c += 2) {
+      load_chunk_keys(x, s0 + (int64_t)c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, s0 + (int64_t)(c + 1) * kSelChunk, s1, t, kb);
+      scatter(ka, s0 + (int64_t)c * kSelChunk);
+      scatter(kb, s0 + (int64_t)(c + 1) * kSelChunk);
     }
-    __syncthreads();
   }
+  cluster_sync_all();  // the candidates are in the leader; no remote access follows
+  if (part != 0) return;
+
+  // ---- 3. the leader finds the exact remainder inside b1
+  const uint32_t nb1 = sm.all_eq;
+  const uint32_t need = k - above;
   if (t == 0) sm.slot = above;
   __syncthreads();
-
-  // ---- 3. the exact remainder inside b1
-  const uint32_t nb1 = sm.n_cand;
-  const uint32_t need = k - above;
   auto emit = [&](uint32_t, int32_t i) {
     const uint32_t s = warp_claim(&sm.slot, true);
     if (s < k) out[s] = i;
   };
-  if (nb1 <= (uint32_t)kSelCandCap) {
+  if (nb1 <= (uint32_t)kCandSmem) {
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
     radix_select(sm.hist, sm.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
   } else {
+    // more boundary elements than the list holds: radix passes over the row
     const GlobalLogits<true> row{x, 0, len};
     radix_select(sm.hist, sm.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
   }
@@ -219,17 +329,21 @@ __global__ void __launch_bounds__(256) paged_ws_zero_kernel(uint4* w, int64_t n1
 
 }  // namespace
 
-size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k,
-                                  int32_t* tiles_per_cta_out, int32_t* chunks_out) {
+size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k) {
   (void)k;
   if (B <= 0 || (next_n != 1 && next_n != 2) || max_blocks <= 0) return 0;
-  if (tiles_per_cta_out) *tiles_per_cta_out = kFusedTilesPerItem;
-  if (chunks_out)
-    *chunks_out = (int32_t)(((int64_t)max_blocks * kPage + kFusedTilesPerItem * kTileKeys - 1) /
-                            (kFusedTilesPerItem * kTileKeys));
   size_t total = 0;
   ws_layout(nullptr, (int64_t)B * next_n, max_blocks, &total);
   return total;
+}
+
+int32_t paged_topk_item_tiles(int32_t B, int32_t max_blocks, int64_t ctas) {
+  // about eight work items per CTA when every sequence fills its block table
+  // (small items even out the CTAs' finishing times; each item costs the
+  // loader a round of dependent loads, so large batches take larger ones)
+  const int64_t tiles = (int64_t)B * (((int64_t)max_blocks * kPage + kTileKeys - 1) / kTileKeys);
+  const int64_t per = tiles / ((ctas > 0 ? ctas : 1) * 8);
+  return per < 6 ? 4 : (per < 12 ? 8 : 16);
 }
 
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
@@ -237,7 +351,13 @@ cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cuda
   const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr);
   const int64_t n16 = (int64_t)(ws.zero_bytes / 16);
   const unsigned zgrid = (unsigned)((n16 + 256 * 8 - 1) / (256 * 8));
-  cudaError_t e = launch_dependent(paged_ws_zero_kernel, dim3(zgrid), dim3(256), 0, stream,
+  // the three kernels share one shared-memory carveout, so no SM has to be
+  // reconfigured between them
+  cudaError_t e = cudaFuncSetAttribute(paged_ws_zero_kernel,
+                                       cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(paged_ws_zero_kernel, dim3(zgrid), dim3(256), 0, stream,
                                    reinterpret_cast<uint4*>(a.workspace), n16);
   if (e != cudaSuccess) return e;
   // scoring pass: the logits kernel writing into the workspace and counting
@@ -250,12 +370,23 @@ cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cuda
   s.row_hist = ws.hist;
   e = launch_paged_logits(H, next_n, s, stream);
   if (e != cudaSuccess) return e;
+  // select: at most one CTA per SM over all rows (one wave whatever the
+  // cluster placement), each slice >= kMinSlice
+  int64_t parts = (int64_t)(a.sms > 0 ? a.sms : 1) / rows;
+  int64_t by_len = ws.ldw / kMinSlice;
+  by_len = by_len < 1 ? 1 : by_len;
+  parts = parts > by_len ? by_len : parts;
+  parts = parts > kMaxParts ? kMaxParts : (parts < 1 ? 1 : parts);
   const size_t smem = sizeof(SelSmem);
   e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_dependent(paged_select_kernel, dim3((unsigned)rows), dim3(kSelThreads), smem,
-                          stream, a, next_n);
+  return launch_dependent_cluster(paged_select_kernel, dim3((unsigned)(rows * parts)),
+                                  dim3(kSelThreads), smem, stream, (unsigned)parts, a, next_n,
+                                  (int)parts);
 }
 
 }  // namespace idx

@@ -135,3 +135,15 @@ def test_fused_workspace_too_small(idx):
         idx.paged_logits_topk(qv, qs, dev(p.weights), cache, dev(p.block_table),
                               dev(p.context_lens), 1, 32, 2048, workspace=ws)
     assert e.value.status == 3
+
+
+def test_fused_more_sequences_than_the_length_cache(idx, oracle):
+    """Past 1024 sequences the scoring pass hands out work items through its
+    counter instead of equal tile shares: the same result rule holds."""
+    rng = np.random.default_rng(914)
+    lens = [int(x) for x in rng.integers(1, 1200, size=1030)]
+    lens[0], lens[1029] = 4100, 2049
+    p = wl.make_decode("t", 914, lens, 32, 1)
+    g = run_fused(idx, p, 2048)
+    for b, (ol, om, L) in oracle_rows(oracle, p, [0, 517, 1024, 1029]).items():
+        check_topk(g[b], ol[0, :L], om[0, :L], L, 2048, f"seq {b}")

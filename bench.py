@@ -52,7 +52,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--cpu-sample-seqs", type=int, default=1 << 30,
+                    help="sequences of the batch the CPU oracle baseline covers (default: all)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="the CPU oracle baseline repeats decode steps for at least this long")
     ap.add_argument("--no-also", action="store_true",
                     help="skip the secondary insert / prefill measurements")
     ap.add_argument("--ref-budget-s", type=float, default=90.0,
@@ -326,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0:
-        cpu = cpu_baseline(p, args.cpu_sample_seqs)
+        cpu = cpu_baseline(p, args.cpu_sample_seqs, args.cpu_seconds)
 
     if rank != 0:
         return
@@ -435,9 +438,10 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
     }
 
 
-def cpu_baseline(p, n_seq):
+def cpu_baseline(p, n_seq, min_seconds=10.0, max_steps=200):
     """The oracle, as it stands, on the first n_seq sequences of the batch:
-    insert of their new keys, query quantisation, paged logits and top-k."""
+    insert of their new keys, query quantisation, paged logits and top-k,
+    repeated as whole decode steps until at least min_seconds of work."""
     import oracle
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     n_seq = max(1, min(n_seq, p.B))
@@ -447,18 +451,23 @@ def cpu_baseline(p, n_seq):
     old = np.setdiff1d(np.arange(hi_tok), new_rows)
     oracle.quant_insert(p.k[old], p.slots[old], cache)
     rows = n_seq * p.next_n
-    t0 = time.perf_counter()
-    oracle.quant_insert(p.k[new_rows], p.slots[new_rows], cache)
-    qv, qs = oracle.quant_q(p.q[:rows])
     ld = p.block_table.shape[1] * 64
-    lg, _ = oracle.paged_mqa_logits(qv, qs, n_seq, p.next_n, p.H, cache, p.block_table[:n_seq],
-                                    p.context_lens[:n_seq], p.weights[:rows], ld)
     st, en = p.row_windows()
-    oracle.topk_rows(np.nan_to_num(lg, nan=-np.inf), st[:rows], en[:rows], p.topk)
-    dt = time.perf_counter() - t0
     toks = int((en[:rows].astype(np.int64) - st[:rows]).sum())
-    return {"value": toks / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"first {n_seq} of {p.B} sequences ({toks} key-tokens), one decode step",
+    steps, dt = 0, 0.0
+    while steps < max_steps and (steps == 0 or dt < min_seconds):
+        t0 = time.perf_counter()
+        oracle.quant_insert(p.k[new_rows], p.slots[new_rows], cache)
+        qv, qs = oracle.quant_q(p.q[:rows])
+        lg, _ = oracle.paged_mqa_logits(qv, qs, n_seq, p.next_n, p.H, cache, p.block_table[:n_seq],
+                                        p.context_lens[:n_seq], p.weights[:rows], ld)
+        oracle.topk_rows(np.nan_to_num(lg, nan=-np.inf), st[:rows], en[:rows], p.topk)
+        dt += time.perf_counter() - t0
+        steps += 1
+    return {"value": steps * toks / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{steps} decode steps over the first {n_seq} of {p.B} sequences "
+                      f"({toks} key-tokens per step)",
             "seconds": dt}
 
 
@@ -473,7 +482,7 @@ def run_reference(args, rank, world):
     # calibrate the per-step sample so that warmup + steps take about 90 s
     budget_s = args.ref_budget_s
     n_steps = args.steps + args.warmup
-    probe = cpu_baseline(p, 1)
+    probe = cpu_baseline(p, 1, min_seconds=0.0)
     rate = probe["value"]
     per_step_tokens = max(2048, int(rate * budget_s / max(n_steps, 1)))
     # sample: the first sequences whose windows fit per_step_tokens; a window may

@@ -38,7 +38,6 @@ struct PagedArgs {
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only
   uint32_t* item_counter; // zeroed work-item counter: dynamic scheduling; null: static
-  uint32_t* row_hist;     // zeroed [rows][4096] coarse histograms of the valid logits, or null
   idx_device_errors* errors;
 };
 

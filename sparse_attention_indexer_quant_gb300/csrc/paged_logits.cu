@@ -7,14 +7,12 @@
 // The persistent main loop of paged_core.cuh streams each sequence's pages
 // (cp.async) through tcgen05 block-scaled MXF4 MMAs; this file's epilogue forms
 // sum_h w * max(0, D) for each of the next_n query rows of a key and writes it
-// to the logits row (-inf past the window when the rows are clean); for the
-// fused path it also counts the logit into its row's coarse histogram.
+// to the logits row (-inf past the window when the rows are clean).
 #include <math.h>
 
 #include "common.cuh"
 #include "launch.h"
 #include "paged_core.cuh"
-#include "topk_select.cuh"
 
 namespace idx {
 namespace {
@@ -36,16 +34,10 @@ struct UnfusedEpilogue {
     for (int j = 0; j < NEXT_N; ++j) {
       const int64_t len = it.L - NEXT_N + j + 1;
       float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
-      if (key < len) {
+      if (key < len)
         row[key] = logit[j];
-        // the fused path's selection starts from each row's coarse histogram
-        if (p.row_hist != nullptr)
-          atomicAdd(p.row_hist + ((int64_t)it.b * NEXT_N + j) * kCoarseBins +
-                        coarse_bin(float_key(logit[j])),
-                    1u);
-      } else if (p.clean && key < p.ld) {
+      else if (p.clean && key < p.ld)
         row[key] = -INFINITY;
-      }
     }
   }
 

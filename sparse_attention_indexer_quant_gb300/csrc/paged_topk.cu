@@ -3,28 +3,30 @@
 // launches that hand the logits over through the caller's workspace instead of
 // a logits tensor:
 //
-//   1. zero     the work-item counter and the row histograms;
+//   1. zero     the scoring pass's work-item counter;
 //   2. score    the persistent cp.async + tcgen05 logits kernel, taking work items
-//               from the counter, writing each row's valid logits to a
-//               row-major scratch that stays in L2 for these sizes and counting
-//               each logit into its row's coarse histogram (the top 12 bits of
-//               its order-preserving key);
+//               from the counter and writing each row's valid logits to a
+//               row-major scratch that stays in L2 for these sizes;
 //   3. select   one thread-block cluster of P CTAs per row, each CTA over a
-//               slice of the row: the row's histogram gives the bin b1 holding
-//               the k-th largest logit and the count above it; each thread
-//               counts its elements above and in b1, one block scan and one
-//               exchange of CTA totals through distributed shared memory give
-//               every thread its output and candidate slots; the elements above
-//               b1 go straight to the output and b1's elements into the
-//               cluster leader's shared memory, where two 10-bit radix digits
-//               finish the exact selection.
+//               slice of the row held in registers: every CTA builds the coarse
+//               histogram of its slice (the top 12 bits of each logit's
+//               order-preserving key) in shared memory; summed over the
+//               cluster through distributed shared memory it gives the bin b1
+//               holding the k-th largest logit and the count above it; each
+//               thread counts its elements above and in b1, one block scan and
+//               one exchange of CTA totals give every thread its output and
+//               candidate slots; the elements above b1 go straight to the
+//               output and b1's elements into the cluster leader's shared
+//               memory, where two 10-bit radix digits finish the exact
+//               selection.
 // All three are dependent launches, so each one's start overlaps the previous
 // one's tail.
 //
 // Workspace (device, caller-owned), 256-byte aligned pieces: the u32 work-item
-// counter and u32 histograms [rows][4096] (both zeroed per call), then f32
-// logits [rows][ldw], ldw = max_blocks * 64.
+// counter (zeroed per call), then f32 logits [rows][ldw], ldw = max_blocks * 64.
 #include <math.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -38,16 +40,15 @@ constexpr int kSelThreads = 512;
 constexpr int kSelVec = 4;                              // float4 loads per thread per chunk
 constexpr int kSelChunk = kSelThreads * 4 * kSelVec;    // 8192 elements
 constexpr int kCandSmem = 8192;                         // boundary-bin elements in the leader
-constexpr int kMaxParts = 8;                            // portable cluster size
+constexpr int kMaxParts = 4;                            // CTAs per row at most
 constexpr int kMinSlice = 4096;                         // elements per CTA at least
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
 
 struct TopkWs {
   uint32_t* items;    // work-item counter of the scoring pass
-  uint32_t* hist;     // [rows][kCoarseBins]
   float* logits;      // [rows][ldw]
   int64_t ldw;
-  size_t zero_bytes;  // counter + histograms
+  size_t zero_bytes;  // the counter
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
@@ -55,20 +56,20 @@ __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 
 __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t max_blocks,
                                             size_t* total) {
   const int64_t ldw = (int64_t)max_blocks * kPage;
-  const size_t o_hist = 256;
-  const size_t o_lg = o_hist + (size_t)rows * kCoarseBins * 4;
+  const size_t o_lg = 256;
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
   w.items = reinterpret_cast<uint32_t*>(p);
-  w.hist = reinterpret_cast<uint32_t*>(p + o_hist);
   w.logits = reinterpret_cast<float*>(p + o_lg);
   w.ldw = ldw;
-  w.zero_bytes = o_lg;
+  w.zero_bytes = 16;
   if (total) *total = o_lg + ws_align((size_t)rows * ldw * 4);
   return w;
 }
 
 struct SelSmem {
+  uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
+  uint32_t row_bins[kCoarseBins];  // ... and of the row (sum over the cluster)
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
   uint32_t warp_gt[kSelThreads / 32], warp_eq[kSelThreads / 32];
@@ -80,22 +81,14 @@ struct SelSmem {
   int32_t cand_idx[kCandSmem];
 };
 
-// Thread t's 8 histogram bins, highest first: 4095 - 8t down to 4088 - 8t.
-__device__ __forceinline__ void load_bins(const uint32_t* hist, int t, uint32_t (&hb)[8]) {
-  const uint4* h = reinterpret_cast<const uint4*>(hist) + 2 * (kSelThreads - 1 - t);
-  const uint4 lo = __ldcg(h), hi = __ldcg(h + 1);  // bins base..base+3, base+4..base+7
-  hb[0] = hi.w; hb[1] = hi.z; hb[2] = hi.y; hb[3] = hi.x;
-  hb[4] = lo.w; hb[5] = lo.z; hb[6] = lo.y; hb[7] = lo.x;
-}
-
 // Keys of x[i] for this thread's 16 positions of the chunk at `base`
 // (key(-inf) outside [base, s1): its bin lies below the bin of any finite
-// logit, so such positions are neither counted nor taken).
-__device__ __forceinline__ void load_chunk_keys(const float* x, int64_t base, int64_t s1, int t,
+// logit, so such positions are never counted above or in b1).
+__device__ __forceinline__ void load_chunk_keys(const float* x, int32_t base, int32_t s1, int t,
                                                 uint4 (&kv)[kSelVec]) {
 #pragma unroll
   for (int u = 0; u < kSelVec; ++u) {
-    const int64_t i0 = base + 4 * ((int64_t)u * kSelThreads + t);
+    const int32_t i0 = base + 4 * (u * kSelThreads + t);
     float4 v;
     if (i0 + 3 < s1) {
       v = __ldca(reinterpret_cast<const float4*>(x + i0));
@@ -106,6 +99,19 @@ __device__ __forceinline__ void load_chunk_keys(const float* x, int64_t base, in
       v.w = i0 + 3 < s1 ? __ldca(x + i0 + 3) : -INFINITY;
     }
     kv[u] = make_uint4(float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w));
+  }
+}
+
+// Adds the chunk's positions below s1 to the CTA's histogram.
+__device__ __forceinline__ void hist_keys(uint32_t* bins, const uint4 (&kv)[kSelVec], int32_t base,
+                                          int32_t s1, int t) {
+#pragma unroll
+  for (int u = 0; u < kSelVec; ++u) {
+    const int32_t i0 = base + 4 * (u * kSelThreads + t);
+    const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (i0 + q < s1) atomicAdd(&bins[coarse_bin(e4[q])], 1u);
   }
 }
 
@@ -159,12 +165,12 @@ __device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b,
 }
 
 // Launched as clusters of `parts` CTAs, one cluster per row.  Every CTA of a
-// cluster takes the same branches and passes the same two cluster barriers.
-__global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const PagedArgs p, int next_n,
+// cluster takes the same branches and passes the same three cluster barriers.
+__global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const PagedArgs p, int next_n,
                                                                       int parts) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  pdl_wait();  // the scoring pass's logits and histograms
+  pdl_wait();  // the scoring pass's logits
   const int64_t rows = (int64_t)p.B * next_n;
   const TopkWs ws = ws_layout(p.workspace, rows, p.max_blocks, nullptr);
   const int64_t r = blockIdx.x / parts;
@@ -183,55 +189,79 @@ __global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const Page
       for (int i = t; i < (int)k; i += kSelThreads) out[i] = i < len ? i : -1;
     return;
   }
-  const int64_t slice = ((len + parts - 1) / parts + 3) / 4 * 4;
-  const int64_t s0 = (int64_t)part * slice;
-  const int64_t s1 = s0 + slice < len ? s0 + slice : len;
-  const int n_chunks = (int)((slice + kSelChunk - 1) / kSelChunk);
+  // positions within a row fit 32 bits (the output indices are int32)
+  const int32_t n = (int32_t)len;
+  const int32_t slice = ((n + parts - 1) / parts + 3) / 4 * 4;
+  const int32_t s0 = part * slice;
+  const int32_t s1 = s0 + slice < n ? s0 + slice : n;
+  const int n_chunks = (slice + kSelChunk - 1) / kSelChunk;
   const float* x = ws.logits + r * ws.ldw;  // 256-byte aligned; slices 16-byte aligned
 
-  // the first two chunks' loads go out together with the histogram's
   uint4 ka[kSelVec], kb[kSelVec];
   load_chunk_keys(x, s0, s1, t, ka);
   load_chunk_keys(x, s0 + kSelChunk, s1, t, kb);
-
-  // ---- 1. boundary bin from the row's histogram (every CTA of the row)
-  uint32_t b1, above;
-  {
-    uint32_t hb[8];
-    load_bins(ws.hist + r * kCoarseBins, t, hb);
-    if (t == 0) {
-      sm.s.bin = 0;
-      sm.s.above = 0;
-    }
-    uint32_t local = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) local += hb[q];
-    const uint32_t excl = block_exclusive_scan(local, sm.s);
-    if (excl < k && k <= excl + local) {
-      uint32_t run = excl;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (run < k && k <= run + hb[q]) {
-          sm.s.bin = (uint32_t)(kCoarseBins - 1 - 8 * t - q);
-          sm.s.above = run;
-        }
-        run += hb[q];
-      }
-    }
-    __syncthreads();
-    b1 = sm.s.bin;
-    above = sm.s.above;
+  for (int q = 0; q < 8; ++q) sm.bins[8 * t + q] = 0u;
+  if (t == 0) {
+    sm.s.bin = 0;
+    sm.s.above = 0;
   }
+  __syncthreads();
+
+  // ---- 1. coarse histogram of the slice, then of the row
+  hist_keys(sm.bins, ka, s0, s1, t);
+  hist_keys(sm.bins, kb, s0 + kSelChunk, s1, t);
+  for (int c = 2; c < n_chunks; c += 2) {  // (then the later passes reload every chunk)
+    load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
+    load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+    hist_keys(sm.bins, ka, s0 + c * kSelChunk, s1, t);
+    hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
+  }
+  cluster_sync_all();  // #1: every CTA's slice histogram is complete
+  // thread t's bins 4095 - 8t down to 4088 - 8t, summed over the cluster
+  uint32_t local = 0;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {  // 4 bins at a time
+    const uint32_t my = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t + 4 * half]);
+    uint4 acc = ld_cluster_v4(cluster_map(my, 0));
+    for (int q = 1; q < parts; ++q) {
+      const uint4 v = ld_cluster_v4(cluster_map(my, q));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<uint4*>(&sm.row_bins[kCoarseBins - 8 - 8 * t + 4 * half]) = acc;
+    local += acc.x + acc.y + acc.z + acc.w;
+  }
+  const uint32_t excl = block_exclusive_scan(local, sm.s);
+  if (excl < k && k <= excl + local) {
+    uint32_t run = excl;
+    for (int q = 0; q < 8; ++q) {  // bins 4095 - 8t - q, highest first
+      const uint32_t h = sm.row_bins[kCoarseBins - 1 - 8 * t - q];
+      if (run < k && k <= run + h) {
+        sm.s.bin = (uint32_t)(kCoarseBins - 1 - 8 * t - q);
+        sm.s.above = run;
+      }
+      run += h;
+    }
+  }
+  __syncthreads();
+  const uint32_t b1 = sm.s.bin;
+  const uint32_t above = sm.s.above;
 
   // ---- 2a. this thread's counts above b1 and in b1 over the slice
   uint32_t n_gt = 0, n_eq = 0;
-  count_keys(ka, b1, n_gt, n_eq);
-  count_keys(kb, b1, n_gt, n_eq);
-  for (int c = 2; c < n_chunks; c += 2) {  // (then 2c reloads every chunk)
-    load_chunk_keys(x, s0 + (int64_t)c * kSelChunk, s1, t, ka);
-    load_chunk_keys(x, s0 + (int64_t)(c + 1) * kSelChunk, s1, t, kb);
+  if (n_chunks <= 2) {  // still in registers
     count_keys(ka, b1, n_gt, n_eq);
     count_keys(kb, b1, n_gt, n_eq);
+  } else {
+    for (int c = 0; c < n_chunks; c += 2) {
+      load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      count_keys(ka, b1, n_gt, n_eq);
+      count_keys(kb, b1, n_gt, n_eq);
+    }
   }
 
   // ---- 2b. slots: block scan, then the CTAs of the row trade totals
@@ -241,7 +271,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const Page
     sm.cta_gt = tg;
     sm.cta_eq = te;
   }
-  cluster_sync_all();  // every CTA's totals are visible
+  cluster_sync_all();  // #2: every CTA's totals are visible; no CTA reads bins any more
   if (t < 32) {  // lane q reads CTA q's totals, all in flight together
     uint32_t g = 0, e = 0;
     if (t < parts) {
@@ -264,16 +294,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const Page
   const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
   uint32_t o = sm.o_base + eg;
   uint32_t ce = sm.c_base + ee;
-  auto scatter = [&](const uint4 (&kv)[kSelVec], int64_t base) {
+  auto scatter = [&](const uint4 (&kv)[kSelVec], int32_t base) {
 #pragma unroll
     for (int u = 0; u < kSelVec; ++u) {
-      const int64_t i0 = base + 4 * ((int64_t)u * kSelThreads + t);
+      const int32_t i0 = base + 4 * (u * kSelThreads + t);
       const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t bin = coarse_bin(e4[q]);
         if (bin > b1) {
-          if (o < above) out[o] = (int32_t)(i0 + q);
+          if (o < above) out[o] = i0 + q;
           ++o;
         } else if (bin == b1) {
           if (ce < (uint32_t)kCandSmem) {
@@ -285,18 +315,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const Page
       }
     }
   };
-  if (n_chunks <= 2) {  // still in registers
+  if (n_chunks <= 2) {
     scatter(ka, s0);
     scatter(kb, s0 + kSelChunk);
   } else {
     for (int c = 0; c < n_chunks; c += 2) {
-      load_chunk_keys(x, s0 + (int64_t)c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, s0 + (int64_t)(c + 1) * kSelChunk, s1, t, kb);
-      scatter(ka, s0 + (int64_t)c * kSelChunk);
-      scatter(kb, s0 + (int64_t)(c + 1) * kSelChunk);
+      load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      scatter(ka, s0 + c * kSelChunk);
+      scatter(kb, s0 + (c + 1) * kSelChunk);
     }
   }
-  cluster_sync_all();  // the candidates are in the leader; no remote access follows
+  cluster_sync_all();  // #3: the candidates are in the leader; no remote access follows
   if (part != 0) return;
 
   // ---- 3. the leader finds the exact remainder inside b1
@@ -313,18 +343,58 @@ __global__ void __launch_bounds__(kSelThreads, 2) paged_select_kernel(const Page
     radix_select(sm.hist, sm.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
   } else {
     // more boundary elements than the list holds: radix passes over the row
-    const GlobalLogits<true> row{x, 0, len};
+    const GlobalLogits<true> row{x, 0, (int64_t)n};
     radix_select(sm.hist, sm.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
   }
 }
 
-// Zeroes the work-item counter and the row histograms (n16 16-byte words).
-__global__ void __launch_bounds__(256) paged_ws_zero_kernel(uint4* w, int64_t n16) {
+// Zeroes the scoring pass's work-item counter.
+__global__ void __launch_bounds__(32) paged_ws_zero_kernel(uint32_t* counter) {
   pdl_launch_dependents();
-  pdl_wait();  // the previous call's select may still be reading them
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
-       i += (int64_t)gridDim.x * blockDim.x)
-    w[i] = make_uint4(0u, 0u, 0u, 0u);
+  pdl_wait();  // the previous call's kernels are done with the workspace
+  if (threadIdx.x == 0) *counter = 0u;
+}
+
+// Parts per row for the select: the most (up to kMaxParts, slices of at
+// least kMinSlice elements, at most one CTA per SM) for which every row's
+// cluster can be resident at once, so the launch is a single wave.  The
+// cluster capacities come from the occupancy API, once per device.
+int select_parts(int64_t rows, int64_t ldw, int sms, size_t smem) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int capacity[kMaxDevices][kMaxParts + 1];  // 0: not yet asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+  int64_t best = 1;
+  for (int P = 2; P <= kMaxParts; ++P) {
+    if (ldw / P < kMinSlice || rows * P > (int64_t)sms) break;
+    int cap = 0;
+    if (dev >= 0) {
+      std::lock_guard<std::mutex> lock(mu);
+      if (capacity[dev][P] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)P);
+        cfg.blockDim = dim3(kSelThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)P;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, paged_select_kernel, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = -1;
+        }
+        capacity[dev][P] = n > 0 ? n : -1;
+      }
+      cap = capacity[dev][P];
+    }
+    if (cap >= rows) best = P;
+  }
+  return (int)best;
 }
 
 }  // namespace
@@ -349,44 +419,34 @@ int32_t paged_topk_item_tiles(int32_t B, int32_t max_blocks, int64_t ctas) {
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.B * next_n;
   const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr);
-  const int64_t n16 = (int64_t)(ws.zero_bytes / 16);
-  const unsigned zgrid = (unsigned)((n16 + 256 * 8 - 1) / (256 * 8));
+  const size_t smem = sizeof(SelSmem);
   // the three kernels share one shared-memory carveout, so no SM has to be
   // reconfigured between them
   cudaError_t e = cudaFuncSetAttribute(paged_ws_zero_kernel,
                                        cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(paged_ws_zero_kernel, dim3(zgrid), dim3(256), 0, stream,
-                                   reinterpret_cast<uint4*>(a.workspace), n16);
+  e = launch_dependent(paged_ws_zero_kernel, dim3(1), dim3(32), 0, stream, ws.items);
   if (e != cudaSuccess) return e;
-  // scoring pass: the logits kernel writing into the workspace and counting
-  // the row histograms, work items handed out by the counter
+  // scoring pass: the logits kernel writing into the workspace, work items
+  // handed out by the counter
   PagedArgs s = a;
   s.logits = ws.logits;
   s.ld = ws.ldw;
   s.clean = 0;
   s.item_counter = ws.items;
-  s.row_hist = ws.hist;
   e = launch_paged_logits(H, next_n, s, stream);
   if (e != cudaSuccess) return e;
-  // select: at most one CTA per SM over all rows (one wave whatever the
-  // cluster placement), each slice >= kMinSlice
-  int64_t parts = (int64_t)(a.sms > 0 ? a.sms : 1) / rows;
-  int64_t by_len = ws.ldw / kMinSlice;
-  by_len = by_len < 1 ? 1 : by_len;
-  parts = parts > by_len ? by_len : parts;
-  parts = parts > kMaxParts ? kMaxParts : (parts < 1 ? 1 : parts);
-  const size_t smem = sizeof(SelSmem);
-  e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
+  const int parts = select_parts(rows, ws.ldw, a.sms > 0 ? a.sms : 1, smem);
   return launch_dependent_cluster(paged_select_kernel, dim3((unsigned)(rows * parts)),
                                   dim3(kSelThreads), smem, stream, (unsigned)parts, a, next_n,
-                                  (int)parts);
+                                  parts);
 }
 
 }  // namespace idx

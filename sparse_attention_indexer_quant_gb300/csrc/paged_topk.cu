@@ -13,12 +13,13 @@
 //               order-preserving key) in shared memory; summed over the
 //               cluster through distributed shared memory it gives the bin b1
 //               holding the k-th largest logit and the count above it; each
-//               thread counts its elements above and in b1, one block scan and
-//               one exchange of CTA totals give every thread its output and
-//               candidate slots; the elements above b1 go straight to the
-//               output and b1's elements into the cluster leader's shared
-//               memory, where two 10-bit radix digits finish the exact
-//               selection.
+//               CTAs then count b1's elements by the next 8 key bits, which
+//               gives the sub-bin sb1 the same way; each thread counts its
+//               elements above and in (b1, sb1), one block scan and one
+//               exchange of CTA totals give every thread its output and
+//               candidate slots; the elements above (b1, sb1) go straight to
+//               the output and its own few elements into the cluster leader's
+//               shared memory, where they are ranked by key and position.
 // All three are dependent launches, so each one's start overlaps the previous
 // one's tail.
 //
@@ -42,6 +43,8 @@ constexpr int kSelChunk = kSelThreads * 4 * kSelVec;    // 8192 elements
 constexpr int kCandSmem = 8192;                         // boundary-bin elements in the leader
 constexpr int kMaxParts = 4;                            // CTAs per row at most
 constexpr int kMinSlice = 4096;                         // elements per CTA at least
+constexpr int kSubShift = 12;                           // sub-bin: key bits 19..12
+constexpr int kSubBins = 256;
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
 
 struct TopkWs {
@@ -70,6 +73,8 @@ __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t ma
 struct SelSmem {
   uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
   uint32_t row_bins[kCoarseBins];  // ... and of the row (sum over the cluster)
+  uint32_t sub[kSubBins];      // this CTA's b1 elements by the next 8 key bits
+  uint32_t sb1, above2;        // the boundary sub-bin, b1's elements above it
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
   uint32_t warp_gt[kSelThreads / 32], warp_eq[kSelThreads / 32];
@@ -115,20 +120,6 @@ __device__ __forceinline__ void hist_keys(uint32_t* bins, const uint4 (&kv)[kSel
   }
 }
 
-__device__ __forceinline__ void count_keys(const uint4 (&kv)[kSelVec], uint32_t b1, uint32_t& n_gt,
-                                           uint32_t& n_eq) {
-#pragma unroll
-  for (int u = 0; u < kSelVec; ++u) {
-    const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t bin = coarse_bin(e4[q]);
-      n_gt += bin > b1 ? 1u : 0u;
-      n_eq += bin == b1 ? 1u : 0u;
-    }
-  }
-}
-
 // Exclusive prefix sums of a and b over the block's threads (ea, eb) and their
 // block totals (ta, tb).  The caller syncs before the scratch is reused.
 __device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b, uint32_t& ea,
@@ -165,7 +156,7 @@ __device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b,
 }
 
 // Launched as clusters of `parts` CTAs, one cluster per row.  Every CTA of a
-// cluster takes the same branches and passes the same three cluster barriers.
+// cluster takes the same branches and passes the same four cluster barriers.
 __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const PagedArgs p, int next_n,
                                                                       int parts) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -202,18 +193,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   load_chunk_keys(x, s0 + kSelChunk, s1, t, kb);
 #pragma unroll
   for (int q = 0; q < 8; ++q) sm.bins[8 * t + q] = 0u;
+  if (t < kSubBins) sm.sub[t] = 0u;
   if (t == 0) {
     sm.s.bin = 0;
     sm.s.above = 0;
+    sm.sb1 = 0;
+    sm.above2 = 0;
   }
   __syncthreads();
 
   // ---- 1. coarse histogram of the slice, then of the row
-  hist_keys(sm.bins, ka, s0, s1, t);
-  hist_keys(sm.bins, kb, s0 + kSelChunk, s1, t);
-  for (int c = 2; c < n_chunks; c += 2) {  // (then the later passes reload every chunk)
-    load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
-    load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+  for (int c = 0; c < n_chunks; c += 2) {  // (past two chunks the later passes reload)
+    if (c > 0) {
+      load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+    }
     hist_keys(sm.bins, ka, s0 + c * kSelChunk, s1, t);
     hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
   }
@@ -250,28 +244,104 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   const uint32_t b1 = sm.s.bin;
   const uint32_t above = sm.s.above;
 
-  // ---- 2a. this thread's counts above b1 and in b1 over the slice
-  uint32_t n_gt = 0, n_eq = 0;
-  if (n_chunks <= 2) {  // still in registers
-    count_keys(ka, b1, n_gt, n_eq);
-    count_keys(kb, b1, n_gt, n_eq);
-  } else {
-    for (int c = 0; c < n_chunks; c += 2) {
+  // ---- 2. the boundary sub-bin sb1: b1's elements by key bits 19..12,
+  //         summed over the cluster
+  auto sub_keys = [&](const uint4 (&kv)[kSelVec]) {
+#pragma unroll
+    for (int u = 0; u < kSelVec; ++u) {
+      const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (coarse_bin(e4[q]) == b1) atomicAdd(&sm.sub[(e4[q] >> kSubShift) & (kSubBins - 1)], 1u);
+    }
+  };
+  // every pass below walks the slice two chunks at a time; a slice of at most
+  // two chunks is still in registers, a longer one is read again
+  const bool reload = n_chunks > 2;
+  for (int c = 0; c < n_chunks; c += 2) {
+    if (reload) {
       load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
-      count_keys(ka, b1, n_gt, n_eq);
-      count_keys(kb, b1, n_gt, n_eq);
+    }
+    sub_keys(ka);
+    sub_keys(kb);
+  }
+  cluster_sync_all();  // #2: every CTA's sub-bin counts are complete
+  {
+    uint32_t sv = 0;  // thread t < 256 holds sub-bin 255 - t (highest first)
+    if (t < kSubBins) {
+      const uint32_t my = smem_u32(&sm.sub[kSubBins - 1 - t]);
+      for (int q = 0; q < parts; ++q) sv += ld_cluster_u32(cluster_map(my, q));
+    }
+    const uint32_t need1 = k - above;
+    const uint32_t ex = block_exclusive_scan(sv, sm.s);
+    if (t < kSubBins && ex < need1 && need1 <= ex + sv) {
+      sm.sb1 = (uint32_t)(kSubBins - 1 - t);
+      sm.above2 = ex;
+    }
+    __syncthreads();
+  }
+  const uint32_t sb1 = sm.sb1;
+  const uint32_t taken = above + sm.above2;  // elements above (b1, sb1)
+  // an element goes straight to the output when its (bin, sub-bin) is above
+  // (b1, sb1), and to the candidates when equal to it
+  auto cls = [&](uint32_t key) -> int {
+    const uint32_t bin = coarse_bin(key);
+    if (bin != b1) return bin > b1 ? 1 : 0;
+    const uint32_t sub = (key >> kSubShift) & (kSubBins - 1);
+    return sub > sb1 ? 1 : (sub == sb1 ? 2 : 0);
+  };
+
+  // ---- 3a. this thread's elements above and in (b1, sb1), as bit masks over
+  //         the 32 positions of a chunk pair (bit 16*h + 4*u + q: chunk h,
+  //         float4 u, lane q of it)
+  auto masks = [&](uint32_t& gt, uint32_t& eq) {
+    gt = 0u;
+    eq = 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int u = 0; u < kSelVec; ++u) {
+        const uint4 v = h == 0 ? ka[u] : kb[u];
+        const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = cls(e4[q]);
+          const uint32_t bit = 1u << (16 * h + 4 * u + q);
+          gt |= c == 1 ? bit : 0u;
+          eq |= c == 2 ? bit : 0u;
+        }
+      }
+    }
+  };
+  auto position = [&](int c, int bit) -> int32_t {  // chunk pair c, mask bit
+    return s0 + (c + (bit >> 4)) * kSelChunk + 4 * (((bit >> 2) & 3) * kSelThreads + t) + (bit & 3);
+  };
+  uint32_t n_gt = 0, n_eq = 0;
+  uint32_t gt0 = 0, eq0 = 0;  // the first chunk pair's masks (the only one unless reloading)
+  for (int c = 0; c < n_chunks; c += 2) {
+    if (reload) {
+      load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+    }
+    uint32_t gt, eq;
+    masks(gt, eq);
+    n_gt += __popc(gt);
+    n_eq += __popc(eq);
+    if (c == 0) {
+      gt0 = gt;
+      eq0 = eq;
     }
   }
 
-  // ---- 2b. slots: block scan, then the CTAs of the row trade totals
+  // ---- 3b. slots: block scan, then the CTAs of the row trade totals
   uint32_t eg, ee, tg, te;
   block_scan2(sm, n_gt, n_eq, eg, ee, tg, te);
   if (t == 0) {
     sm.cta_gt = tg;
     sm.cta_eq = te;
   }
-  cluster_sync_all();  // #2: every CTA's totals are visible; no CTA reads bins any more
+  cluster_sync_all();  // #3: every CTA's totals are visible
   if (t < 32) {  // lane q reads CTA q's totals, all in flight together
     uint32_t g = 0, e = 0;
     if (t < parts) {
@@ -289,62 +359,66 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   }
   __syncthreads();
 
-  // ---- 2c. elements above b1 -> out, b1's elements -> the leader's list
+  // ---- 3c. elements above (b1, sb1) -> out, its elements -> the leader's list
   const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
   const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
   uint32_t o = sm.o_base + eg;
   uint32_t ce = sm.c_base + ee;
-  auto scatter = [&](const uint4 (&kv)[kSelVec], int32_t base) {
-#pragma unroll
-    for (int u = 0; u < kSelVec; ++u) {
-      const int32_t i0 = base + 4 * (u * kSelThreads + t);
-      const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t bin = coarse_bin(e4[q]);
-        if (bin > b1) {
-          if (o < above) out[o] = i0 + q;
-          ++o;
-        } else if (bin == b1) {
-          if (ce < (uint32_t)kCandSmem) {
-            st_cluster_u32(cand_keys0 + 4u * ce, e4[q]);
-            st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)(i0 + q));
-          }
-          ++ce;
-        }
-      }
-    }
-  };
-  if (n_chunks <= 2) {
-    scatter(ka, s0);
-    scatter(kb, s0 + kSelChunk);
-  } else {
-    for (int c = 0; c < n_chunks; c += 2) {
+  for (int c = 0; c < n_chunks; c += 2) {
+    uint32_t gt = gt0, eq = eq0;
+    if (c > 0) {  // (reloading; the masks of pair 0 are kept)
       load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
-      scatter(ka, s0 + c * kSelChunk);
-      scatter(kb, s0 + (c + 1) * kSelChunk);
+      masks(gt, eq);
+    }
+    for (; gt != 0u; gt &= gt - 1u) {
+      if (o < taken) out[o] = position(c, __ffs(gt) - 1);
+      ++o;
+    }
+    for (; eq != 0u; eq &= eq - 1u) {
+      const int32_t i = position(c, __ffs(eq) - 1);
+      if (ce < (uint32_t)kCandSmem) {
+        st_cluster_u32(cand_keys0 + 4u * ce, float_key(__ldca(x + i)));
+        st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)i);
+      }
+      ++ce;
     }
   }
-  cluster_sync_all();  // #3: the candidates are in the leader; no remote access follows
+  cluster_sync_all();  // #4: the candidates are in the leader; no remote access follows
   if (part != 0) return;
 
-  // ---- 3. the leader finds the exact remainder inside b1
-  const uint32_t nb1 = sm.all_eq;
-  const uint32_t need = k - above;
-  if (t == 0) sm.slot = above;
+  // ---- 4. the leader takes the remaining k - taken of the candidates, which
+  //         share their top 20 key bits: by rank (key, then position) when
+  //         there are few, else by a radix digit on the low 12 bits
+  const uint32_t nb = sm.all_eq;
+  const uint32_t need = k - taken;
+  if (nb <= (uint32_t)kSelThreads) {
+    if ((uint32_t)t < nb) {
+      const uint32_t key = sm.cand_keys[t];
+      const int32_t pos = sm.cand_idx[t];
+      uint32_t rank = 0;
+      for (uint32_t q = 0; q < nb; ++q) {
+        const uint32_t kq = sm.cand_keys[q];
+        rank += (kq > key || (kq == key && sm.cand_idx[q] < pos)) ? 1u : 0u;
+      }
+      if (rank < need) out[taken + rank] = pos;
+    }
+    return;
+  }
+  if (t == 0) sm.slot = taken;
   __syncthreads();
   auto emit = [&](uint32_t, int32_t i) {
     const uint32_t s = warp_claim(&sm.slot, true);
     if (s < k) out[s] = i;
   };
-  if (nb1 <= (uint32_t)kCandSmem) {
-    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
-    radix_select(sm.hist, sm.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+  const uint32_t prefix = (b1 << kCoarseShift) | (sb1 << kSubShift);
+  if (nb <= (uint32_t)kCandSmem) {
+    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb};
+    radix_select(sm.hist, sm.s, cand, need, prefix, 32 - kSubShift, emit);
   } else {
-    // more boundary elements than the list holds: radix passes over the row
+    // more such elements than the list holds: a radix pass over the row
     const GlobalLogits<true> row{x, 0, (int64_t)n};
-    radix_select(sm.hist, sm.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+    radix_select(sm.hist, sm.s, row, need, prefix, 32 - kSubShift, emit);
   }
 }
 

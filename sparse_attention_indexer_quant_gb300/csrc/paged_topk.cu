@@ -45,6 +45,7 @@ constexpr int kMaxParts = 4;                            // CTAs per row at most
 constexpr int kMinSlice = 4096;                         // elements per CTA at least
 constexpr int kSubShift = 12;                           // sub-bin: key bits 19..12
 constexpr int kSubBins = 256;
+constexpr int kMaskPairs = 8;                           // chunk pairs whose masks are kept
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
 
 struct TopkWs {
@@ -74,6 +75,8 @@ struct SelSmem {
   uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
   uint32_t row_bins[kCoarseBins];  // ... and of the row (sum over the cluster)
   uint32_t sub[kSubBins];      // this CTA's b1 elements by the next 8 key bits
+  uint32_t mgt[kMaskPairs][kSelThreads];  // per thread and chunk pair: taken outright
+  uint32_t meq[kMaskPairs][kSelThreads];  // ... and boundary candidates
   uint32_t sb1, above2;        // the boundary sub-bin, b1's elements above it
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
@@ -212,19 +215,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
     hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
   }
   cluster_sync_all();  // #1: every CTA's slice histogram is complete
-  // thread t's bins 4095 - 8t down to 4088 - 8t, summed over the cluster
+  // thread t's bins 4095 - 8t down to 4088 - 8t, summed over the cluster (all
+  // of a thread's remote loads are issued before any is used)
   uint32_t local = 0;
-#pragma unroll 1
+#pragma unroll
   for (int half = 0; half < 2; ++half) {  // 4 bins at a time
     const uint32_t my = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t + 4 * half]);
-    uint4 acc = ld_cluster_v4(cluster_map(my, 0));
-    for (int q = 1; q < parts; ++q) {
-      const uint4 v = ld_cluster_v4(cluster_map(my, q));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 v0 = ld_cluster_v4(cluster_map(my, 0));
+    const uint4 v1 = parts > 1 ? ld_cluster_v4(cluster_map(my, 1)) : z;
+    const uint4 v2 = parts > 2 ? ld_cluster_v4(cluster_map(my, 2)) : z;
+    const uint4 v3 = parts > 3 ? ld_cluster_v4(cluster_map(my, 3)) : z;
+    const uint4 acc = make_uint4(v0.x + v1.x + v2.x + v3.x, v0.y + v1.y + v2.y + v3.y,
+                                 v0.z + v1.z + v2.z + v3.z, v0.w + v1.w + v2.w + v3.w);
     *reinterpret_cast<uint4*>(&sm.row_bins[kCoarseBins - 8 - 8 * t + 4 * half]) = acc;
     local += acc.x + acc.y + acc.z + acc.w;
   }
@@ -244,34 +247,62 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   const uint32_t b1 = sm.s.bin;
   const uint32_t above = sm.s.above;
 
-  // ---- 2. the boundary sub-bin sb1: b1's elements by key bits 19..12,
-  //         summed over the cluster
-  auto sub_keys = [&](const uint4 (&kv)[kSelVec]) {
+  // Each thread's elements of a chunk pair are 32 mask bits: bit 16*h + 4*u + q
+  // is chunk h of the pair, float4 u, lane q of it.
+  auto position = [&](int c, int bit) -> int32_t {  // chunk pair starting at chunk c
+    return s0 + (c + (bit >> 4)) * kSelChunk + 4 * (((bit >> 2) & 3) * kSelThreads + t) + (bit & 3);
+  };
+  // masks of the elements above b1 and in b1; b1's elements also counted by
+  // their next 8 key bits
+  auto coarse_masks = [&](uint32_t& gt, uint32_t& eq, bool count_sub) {
+    gt = 0u;
+    eq = 0u;
 #pragma unroll
-    for (int u = 0; u < kSelVec; ++u) {
-      const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (coarse_bin(e4[q]) == b1) atomicAdd(&sm.sub[(e4[q] >> kSubShift) & (kSubBins - 1)], 1u);
+      for (int u = 0; u < kSelVec; ++u) {
+        const uint4 v = h == 0 ? ka[u] : kb[u];
+        const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t bin = coarse_bin(e4[q]);
+          const uint32_t bit = 1u << (16 * h + 4 * u + q);
+          gt |= bin > b1 ? bit : 0u;
+          if (bin == b1) {
+            eq |= bit;
+            if (count_sub) atomicAdd(&sm.sub[(e4[q] >> kSubShift) & (kSubBins - 1)], 1u);
+          }
+        }
+      }
     }
   };
-  // every pass below walks the slice two chunks at a time; a slice of at most
-  // two chunks is still in registers, a longer one is read again
+
+  // ---- 2. the boundary sub-bin sb1: b1's elements by key bits 19..12,
+  //         summed over the cluster; the coarse masks are kept (up to
+  //         kMaskPairs chunk pairs) for the passes below
   const bool reload = n_chunks > 2;
   for (int c = 0; c < n_chunks; c += 2) {
     if (reload) {
       load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
     }
-    sub_keys(ka);
-    sub_keys(kb);
+    uint32_t gt, eq;
+    coarse_masks(gt, eq, true);
+    if (c / 2 < kMaskPairs) {
+      sm.mgt[c / 2][t] = gt;
+      sm.meq[c / 2][t] = eq;
+    }
   }
   cluster_sync_all();  // #2: every CTA's sub-bin counts are complete
   {
     uint32_t sv = 0;  // thread t < 256 holds sub-bin 255 - t (highest first)
     if (t < kSubBins) {
       const uint32_t my = smem_u32(&sm.sub[kSubBins - 1 - t]);
-      for (int q = 0; q < parts; ++q) sv += ld_cluster_u32(cluster_map(my, q));
+      const uint32_t v0 = ld_cluster_u32(cluster_map(my, 0));
+      const uint32_t v1 = parts > 1 ? ld_cluster_u32(cluster_map(my, 1)) : 0u;
+      const uint32_t v2 = parts > 2 ? ld_cluster_u32(cluster_map(my, 2)) : 0u;
+      const uint32_t v3 = parts > 3 ? ld_cluster_u32(cluster_map(my, 3)) : 0u;
+      sv = v0 + v1 + v2 + v3;
     }
     const uint32_t need1 = k - above;
     const uint32_t ex = block_exclusive_scan(sv, sm.s);
@@ -283,54 +314,37 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   }
   const uint32_t sb1 = sm.sb1;
   const uint32_t taken = above + sm.above2;  // elements above (b1, sb1)
-  // an element goes straight to the output when its (bin, sub-bin) is above
-  // (b1, sb1), and to the candidates when equal to it
-  auto cls = [&](uint32_t key) -> int {
-    const uint32_t bin = coarse_bin(key);
-    if (bin != b1) return bin > b1 ? 1 : 0;
-    const uint32_t sub = (key >> kSubShift) & (kSubBins - 1);
-    return sub > sb1 ? 1 : (sub == sb1 ? 2 : 0);
-  };
 
-  // ---- 3a. this thread's elements above and in (b1, sb1), as bit masks over
-  //         the 32 positions of a chunk pair (bit 16*h + 4*u + q: chunk h,
-  //         float4 u, lane q of it)
-  auto masks = [&](uint32_t& gt, uint32_t& eq) {
-    gt = 0u;
-    eq = 0u;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int u = 0; u < kSelVec; ++u) {
-        const uint4 v = h == 0 ? ka[u] : kb[u];
-        const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = cls(e4[q]);
-          const uint32_t bit = 1u << (16 * h + 4 * u + q);
-          gt |= c == 1 ? bit : 0u;
-          eq |= c == 2 ? bit : 0u;
-        }
-      }
-    }
-  };
-  auto position = [&](int c, int bit) -> int32_t {  // chunk pair c, mask bit
-    return s0 + (c + (bit >> 4)) * kSelChunk + 4 * (((bit >> 2) & 3) * kSelThreads + t) + (bit & 3);
-  };
-  uint32_t n_gt = 0, n_eq = 0;
-  uint32_t gt0 = 0, eq0 = 0;  // the first chunk pair's masks (the only one unless reloading)
-  for (int c = 0; c < n_chunks; c += 2) {
-    if (reload) {
+  // ---- 3a. final masks: an element is taken outright when its (bin, sub-bin)
+  //         is above (b1, sb1), a candidate when equal to it; only b1's few
+  //         elements need their sub-bin, read back from the logits
+  auto final_masks = [&](int c, uint32_t& gt, uint32_t& eq) {
+    if (c / 2 < kMaskPairs) {
+      gt = sm.mgt[c / 2][t];
+      eq = sm.meq[c / 2][t];
+    } else {
       load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      coarse_masks(gt, eq, false);
     }
+    uint32_t in = 0u;
+    for (uint32_t m = eq; m != 0u; m &= m - 1u) {
+      const int bit = __ffs(m) - 1;
+      const uint32_t sub = (float_key(__ldca(x + position(c, bit))) >> kSubShift) & (kSubBins - 1);
+      if (sub > sb1) gt |= 1u << bit;
+      else if (sub == sb1) in |= 1u << bit;
+    }
+    eq = in;
+  };
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int c = 0; c < n_chunks; c += 2) {
     uint32_t gt, eq;
-    masks(gt, eq);
+    final_masks(c, gt, eq);
     n_gt += __popc(gt);
     n_eq += __popc(eq);
-    if (c == 0) {
-      gt0 = gt;
-      eq0 = eq;
+    if (c / 2 < kMaskPairs) {
+      sm.mgt[c / 2][t] = gt;
+      sm.meq[c / 2][t] = eq;
     }
   }
 
@@ -365,11 +379,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   uint32_t o = sm.o_base + eg;
   uint32_t ce = sm.c_base + ee;
   for (int c = 0; c < n_chunks; c += 2) {
-    uint32_t gt = gt0, eq = eq0;
-    if (c > 0) {  // (reloading; the masks of pair 0 are kept)
-      load_chunk_keys(x, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, s0 + (c + 1) * kSelChunk, s1, t, kb);
-      masks(gt, eq);
+    uint32_t gt, eq;
+    if (c / 2 < kMaskPairs) {
+      gt = sm.mgt[c / 2][t];
+      eq = sm.meq[c / 2][t];
+    } else {
+      final_masks(c, gt, eq);
     }
     for (; gt != 0u; gt &= gt - 1u) {
       if (o < taken) out[o] = position(c, __ffs(gt) - 1);

@@ -7,7 +7,9 @@
 // butterfly shuffles on the integer bit patterns (for non-negative floats the
 // bit order is the value order).  Each thread then encodes its 8 values into
 // 4 packed bytes and stores one 32-bit word; the block leader gathers the 4
-// scale bytes into one 32-bit word.
+// scale bytes into one 32-bit word.  Both kernels are dependent launches: they
+// are scheduled while the previous kernel finishes and wait for it before
+// reading their inputs.
 #include "common.cuh"
 #include "launch.h"
 
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(kBlockThreads) quant_insert_kernel(
   const bool live = vec < n_tokens;
   int64_t slot = -1;
   uint4 raw = make_uint4(0, 0, 0, 0);
+  pdl_launch_dependents();
+  pdl_wait();  // inputs may come from the previous kernel
   if (live) {
     slot = __ldg(slots + vec);
     raw = __ldg(reinterpret_cast<const uint4*>(k + vec * row_stride) + part);
@@ -91,6 +95,8 @@ __global__ void __launch_bounds__(kBlockThreads) quant_q_kernel(const uint16_t* 
   const int part = threadIdx.x % kThreadsPerVec;
   const bool live = vec < rows;
   uint4 raw = make_uint4(0, 0, 0, 0);
+  pdl_launch_dependents();
+  pdl_wait();  // inputs may come from the previous kernel
   if (live) raw = __ldg(reinterpret_cast<const uint4*>(q + vec * kHeadDim) + part);
   uint32_t sw;
   const uint32_t packed = encode8(raw, &sw);
@@ -106,19 +112,17 @@ cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_str
                                 idx_device_errors* errors, cudaStream_t stream) {
   if (n_tokens == 0) return cudaSuccess;
   const int64_t blocks = (n_tokens + kVecsPerBlock - 1) / kVecsPerBlock;
-  quant_insert_kernel<<<(unsigned)blocks, kBlockThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(k), n_tokens, row_stride, slots, cache,
-      num_blocks * kPage, errors);
-  return cudaGetLastError();
+  return launch_dependent(quant_insert_kernel, dim3((unsigned)blocks), dim3(kBlockThreads), 0,
+                          stream, static_cast<const uint16_t*>(k), n_tokens, row_stride, slots,
+                          cache, num_blocks * kPage, errors);
 }
 
 cudaError_t launch_quant_q(const void* q, int64_t rows, uint8_t* vals, uint8_t* scales,
                            cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + kVecsPerBlock - 1) / kVecsPerBlock;
-  quant_q_kernel<<<(unsigned)blocks, kBlockThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(q), rows, vals, scales);
-  return cudaGetLastError();
+  return launch_dependent(quant_q_kernel, dim3((unsigned)blocks), dim3(kBlockThreads), 0, stream,
+                          static_cast<const uint16_t*>(q), rows, vals, scales);
 }
 
 }  // namespace idx

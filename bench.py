@@ -41,7 +41,7 @@ TOPK = 2048
 L2_FLUSH_BYTES = 256 << 20   # 2x the 129 MB L2
 # sources of the fused decode entry (scoring + select launches); the committed
 # traffic figure is only used while their digest matches
-FUSED_SOURCES = ["paged_topk.cu", "paged_logits.cu", "paged_core.cuh",
+FUSED_SOURCES = ["paged_topk.cu", "paged_logits.cu", "paged_core.cuh", "select_row.cuh",
                  "topk_select.cuh", "common.cuh"]
 
 

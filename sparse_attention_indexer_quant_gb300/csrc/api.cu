@@ -283,11 +283,13 @@ idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const in
   if (rows < 0 || rows > (int64_t)INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "rows=%lld", (long long)rows);
   if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
   if (ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld", (long long)ld);
-  idx_status s = current_device_ok(nullptr);
+  int sms = 0;
+  idx_status s = current_device_ok(&sms);
   if (s != IDX_OK) return s;
   if (rows == 0) return ok();
   if (!logits || !row_end || !out_idx) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
-  return from_cuda(idx::launch_topk_rows(logits, rows, ld, row_start, row_end, k, out_idx,
+  if (!aligned(logits, 4)) return fail(IDX_ERR_INVALID_ARG, "logits not 4-byte aligned");
+  return from_cuda(idx::launch_topk_rows(logits, rows, ld, row_start, row_end, k, out_idx, sms,
                                          (cudaStream_t)stream),
                    "topk_rows launch");
 }

@@ -109,7 +109,7 @@ cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs&
 
 cudaError_t launch_topk_rows(const float* logits, int64_t rows, int64_t ld,
                              const int32_t* row_start, const int32_t* row_end, int32_t k,
-                             int32_t* out, cudaStream_t stream);
+                             int32_t* out, int sms, cudaStream_t stream);
 
 cudaError_t launch_gather_k(const uint8_t* cache, int64_t num_blocks, const int32_t* block_table,
                             int32_t max_blocks, const int32_t* seq_lens,

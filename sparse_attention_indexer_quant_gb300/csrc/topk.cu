@@ -1,23 +1,45 @@
 // Top-k per logits row (vLLM API docs "vllm.models.glm5next.nvidia.sparse_indexer":
 // top_k_per_row into topk_indices_buffer; rows shorter than k are padded with
-// -1): one CTA per row running row_topk over the row's window.
+// -1).  Two kernels, chosen by the number of rows:
+//   - up to one row per SM: one thread-block cluster of P CTAs per row running
+//     cluster_select_row (select_row.cuh), so that a few long rows use the
+//     whole GPU;
+//   - more rows: one 512-thread CTA per row running row_topk (topk_row.cuh),
+//     two CTAs per SM, for throughput over many rows.
 #include "common.cuh"
 #include "launch.h"
+#include "select_row.cuh"
 #include "topk_row.cuh"
 
 namespace idx {
 namespace {
 
+__global__ void __launch_bounds__(kSelThreads, 1)
+    topk_rows_cluster_kernel(const float* __restrict__ logits, int64_t ld,
+                             const int32_t* row_start, const int32_t* row_end, int32_t k,
+                             int32_t* out, int parts) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  pdl_wait();  // the logits may come from the previous kernel
+  const int64_t row = blockIdx.x / parts;
+  const int64_t st = row_start != nullptr ? __ldg(row_start + row) : 0;
+  const int64_t en = __ldg(row_end + row);
+  // positions are reported relative to the window start
+  cluster_select_row(sm, logits + row * ld + st, en > st ? en - st : 0, (uint32_t)k,
+                     out + row * k, parts);
+}
+
 constexpr int kRowsChunk = 8192;
 using RowsSmem = RowTopkSmem<kRowsChunk>;
 
 __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const float* __restrict__ logits,
-                                                                    int64_t ld,
-                                                                    const int32_t* row_start,
-                                                                    const int32_t* row_end,
-                                                                    int32_t k, int32_t* out) {
+                                                                int64_t ld,
+                                                                const int32_t* row_start,
+                                                                const int32_t* row_end,
+                                                                int32_t k, int32_t* out) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   RowsSmem& sm = *reinterpret_cast<RowsSmem*>(smem_raw);
+  pdl_wait();  // the logits may come from the previous kernel
   const int64_t row = blockIdx.x;
   const int64_t st = row_start != nullptr ? __ldg(row_start + row) : 0;
   const int64_t en = __ldg(row_end + row);
@@ -29,15 +51,29 @@ __global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const float* __r
 
 cudaError_t launch_topk_rows(const float* logits, int64_t rows, int64_t ld,
                              const int32_t* row_start, const int32_t* row_end, int32_t k,
-                             int32_t* out, cudaStream_t stream) {
+                             int32_t* out, int sms, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const size_t smem = sizeof(RowsSmem);
-  cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
+  if (sms <= 0) sms = 1;
+  if (rows > sms) {
+    const size_t smem = sizeof(RowsSmem);
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(topk_rows_kernel, dim3((unsigned)rows), dim3(kRowThreads), smem,
+                            stream, logits, ld, row_start, row_end, k, out);
+  }
+  const size_t smem = sizeof(SelSmem);
+  cudaError_t e = cudaFuncSetAttribute(topk_rows_cluster_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_rows_cluster_kernel,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  topk_rows_kernel<<<(unsigned)rows, kRowThreads, smem, stream>>>(logits, ld, row_start, row_end,
-                                                                   k, out);
-  return cudaGetLastError();
+  const int parts = select_parts(topk_rows_cluster_kernel, 1, rows, ld, sms, smem);
+  return launch_dependent_cluster(topk_rows_cluster_kernel, dim3((unsigned)(rows * parts)),
+                                  dim3(kSelThreads), smem, stream, (unsigned)parts, logits, ld,
+                                  row_start, row_end, k, out, parts);
 }
 
 }  // namespace idx

@@ -82,3 +82,28 @@ def test_topk_causal_prefill_rows(idx):
     for t in [0, 1, 2046, 2047, 2048, 2049, 2999]:
         vals = logits[t, :t + 1].astype(np.float64)
         check_topk(out[t], vals, np.zeros_like(vals), t + 1, 2048, f"t={t}")
+
+
+@pytest.mark.parametrize("n,finite", [(20000, 1000), (9000, 100), (131072, 1500)])
+def test_topk_rows_mostly_neg_inf(idx, n, finite):
+    """Rows whose k-th largest value is -inf, long enough to be split over
+    several CTAs, with unaligned window starts: every index must be distinct,
+    inside the window, and cover all finite values."""
+    g = wl.rng(430 + n)
+    k = 2048
+    rows = 3
+    starts = np.array([0, 1, 3])
+    ld = n + 8
+    logits = np.full((rows, ld), np.nan, np.float32)
+    for r in range(rows):
+        row = np.full(n, -np.inf, np.float32)
+        pos = g.choice(n, size=finite, replace=False)
+        row[pos] = g.standard_normal(finite).astype(np.float32)
+        logits[r, starts[r]:starts[r] + n] = row
+    out = run(idx, logits, starts, starts + n, k)
+    for r in range(rows):
+        vals = logits[r, starts[r]:starts[r] + n].astype(np.float64)
+        check_topk(out[r], vals, np.zeros_like(vals), n, k, f"row {r}")
+        assert len(set(out[r].tolist())) == k
+        if finite <= k:
+            assert set(np.nonzero(np.isfinite(vals))[0].tolist()) <= set(out[r].tolist())

@@ -284,23 +284,33 @@ def run_ours(args, rank, world, local_rank):
     total_ms = sum(step_ms)
     total_ms_max = reduce_max(total_ms, world, dev)
 
-    # ---- end to end through the public API with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_new_k = bf16_tensor(p.k[new_rows], "cpu").pin_memory()
-    h_new_slots = pin(p.slots[new_rows])
-    h_q = bf16_tensor(p.q, "cpu").pin_memory()
-    h_w, h_bt, h_cl = pin(p.weights), pin(p.block_table), pin(p.context_lens)
+    # ---- end to end through the public API with host buffers: the step's
+    # inputs live in one pinned staging buffer (16-byte aligned sections), so
+    # one host->device copy carries them all; the indices come back in one copy
+    host_parts = [bf16_tensor(p.k[new_rows], "cpu"), torch.from_numpy(p.slots[new_rows]),
+                  bf16_tensor(p.q, "cpu"), torch.from_numpy(p.weights),
+                  torch.from_numpy(p.block_table), torch.from_numpy(p.context_lens)]
+    offs, total = [], 0
+    for t in host_parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 15) // 16 * 16
+    h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def section(buf, i):
+        t = host_parts[i]
+        n = t.numel() * t.element_size()
+        return buf[offs[i]:offs[i] + n].view(t.dtype).view(t.shape)
+
+    for i, t in enumerate(host_parts):
+        section(h_stage, i).copy_(t)
+    d_new_k, d_new_slots, d_q, d_w, d_bt, d_cl = (section(d_stage, i) for i in range(6))
     h_out = torch.empty((p.rows, TOPK), dtype=torch.int32).pin_memory()
-    d_new_k, d_new_slots = torch.empty_like(new_k), torch.empty_like(new_slots)
-    d_q, d_w, d_bt, d_cl = (torch.empty_like(q), torch.empty_like(w), torch.empty_like(bt),
-                            torch.empty_like(cl))
-    h2d = sum(t.numel() * t.element_size() for t in (h_new_k, h_new_slots, h_q, h_w, h_bt, h_cl))
+    h2d = total
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        for d, h in ((d_new_k, h_new_k), (d_new_slots, h_new_slots), (d_q, h_q), (d_w, h_w),
-                     (d_bt, h_bt), (d_cl, h_cl)):
-            d.copy_(h, non_blocking=True)
+        d_stage.copy_(h_stage, non_blocking=True)
         idx.quant_insert(d_new_k, d_new_slots, cache)
         idx.quant_q(d_q, out_vals=qv, out_scales=qs)
         idx.paged_logits_topk(qv, qs, d_w, cache, d_bt, d_cl, p.next_n, p.H, TOPK,

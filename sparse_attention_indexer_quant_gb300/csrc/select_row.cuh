@@ -7,14 +7,16 @@
 //      each value's order-preserving key) in shared memory; summed over the
 //      cluster through distributed shared memory it gives the bin b1 holding
 //      the k-th largest value and the count above it;
-//   2. the CTAs count b1's elements by the next 8 key bits, which gives the
-//      sub-bin sb1 the same way;
-//   3. each thread classifies its elements as above (b1, sb1) or in it (bit
-//      masks), one block scan and one exchange of CTA totals give every thread
-//      its output and candidate slots; the elements above go straight to the
-//      output, the few in (b1, sb1) into the cluster leader's shared memory;
-//   4. the leader ranks the candidates by key and position (a radix pass on the
-//      low 12 bits when there are many).
+//   2. each thread classifies its elements as above b1 or in it (bit masks);
+//      one block scan and one exchange of CTA totals give every thread its
+//      output and candidate slots; the elements above go straight to the
+//      output, b1's elements (a few hundred for smooth rows) with their keys
+//      into the cluster leader's shared memory;
+//   3. the leader takes the remaining ones from the candidates: by their next
+//      8 key bits (the sub-bin holding the k-th largest), then among that
+//      sub-bin's elements by rank (key, then position), or by a radix digit
+//      on the low 12 bits when there are many.  A boundary bin larger than
+//      the candidate list is resolved by radix passes over the row.
 // Output positions are relative to the row start, in no particular order;
 // equal values may be taken in any order.
 #pragma once
@@ -37,6 +39,8 @@ constexpr int kMinSlice = 4096;                         // elements per CTA at l
 constexpr int kSubShift = 12;                           // sub-bin: key bits 19..12
 constexpr int kSubBins = 256;
 constexpr int kMaskPairs = 8;                           // chunk pairs whose masks are kept
+constexpr int kList2 = kMaskPairs * kSelThreads;        // boundary sub-bin list (the mask space)
+constexpr int kRankDirect = 64;                         // sub-bin lists ranked element by element
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
 
 struct SelSmem {
@@ -45,7 +49,7 @@ struct SelSmem {
   uint32_t sub[kSubBins];      // this CTA's b1 elements by the next 8 key bits
   uint32_t mgt[kMaskPairs][kSelThreads];  // per thread and chunk pair: taken outright
   uint32_t meq[kMaskPairs][kSelThreads];  // ... and boundary candidates
-  uint32_t sb1, above2;        // the boundary sub-bin, b1's elements above it
+  uint32_t n2;                 // candidates in the boundary sub-bin (leader)
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
   uint32_t warp_gt[kSelThreads / 32], warp_eq[kSelThreads / 32];
@@ -77,6 +81,20 @@ __device__ __forceinline__ void load_chunk_keys(const float* x, bool aligned, in
     }
     kv[u] = make_uint4(float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w));
   }
+}
+
+// Key of mask bit `bit` of a chunk pair held in registers (chunk bit >> 4,
+// float4 (bit >> 2) & 3, lane bit & 3), by selects rather than an indexed
+// (local-memory) array access.
+__device__ __forceinline__ uint32_t pair_key(const uint4 (&ka)[kSelVec], const uint4 (&kb)[kSelVec],
+                                             int bit) {
+  static_assert(kSelVec == 4, "four float4 per chunk");
+  const bool u0 = (bit & 4) != 0, u1 = (bit & 8) != 0;
+  const uint4 a = u1 ? (u0 ? ka[3] : ka[2]) : (u0 ? ka[1] : ka[0]);
+  const uint4 b = u1 ? (u0 ? kb[3] : kb[2]) : (u0 ? kb[1] : kb[0]);
+  const uint4 v = (bit & 16) ? b : a;
+  const uint32_t lo = (bit & 1) ? v.y : v.x, hi = (bit & 1) ? v.w : v.z;
+  return (bit & 2) ? hi : lo;
 }
 
 // Adds the chunk's positions below s1 to the CTA's histogram.
@@ -130,7 +148,7 @@ __device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b,
 // The k largest of x[0, len) -> out[0, k) (positions, -1 padded).  Called by
 // every thread of every CTA of a cluster of `parts` CTAs (kSelThreads each)
 // with the same arguments; every CTA takes the same branches and passes the
-// same four cluster barriers.
+// same three cluster barriers.
 __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, int64_t len,
                                                    uint32_t k, int32_t* out, int parts) {
   const int part = (int)cluster_ctarank();
@@ -157,8 +175,7 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   if (t == 0) {
     sm.s.bin = 0;
     sm.s.above = 0;
-    sm.sb1 = 0;
-    sm.above2 = 0;
+    sm.n2 = 0;
   }
   __syncthreads();
 
@@ -202,18 +219,17 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   }
   __syncthreads();
   const uint32_t b1 = sm.s.bin;
-  const uint32_t above = sm.s.above;
+  const uint32_t above = sm.s.above;  // the row's elements in bins above b1
 
   // Each thread's elements of a chunk pair are 32 mask bits: bit 16*h + 4*u + q
   // is chunk h of the pair, float4 u, lane q of it.
   auto position = [&](int c, int bit) -> int32_t {  // chunk pair starting at chunk c
     return s0 + (c + (bit >> 4)) * kSelChunk + 4 * (((bit >> 2) & 3) * kSelThreads + t) + (bit & 3);
   };
-  // masks of the elements above b1 and in b1; b1's elements also counted by
-  // their next 8 key bits
-  // (positions past the slice are skipped: their key(-inf) padding is in b1
-  // when the row's k-th largest value is itself -inf)
-  auto coarse_masks = [&](int c, uint32_t& gt, uint32_t& eq, bool count_sub) {
+  // masks of the elements above b1 and in b1 (positions past the slice are
+  // skipped: their key(-inf) padding is in b1 when the row's k-th largest
+  // value is itself -inf)
+  auto coarse_masks = [&](int c, uint32_t& gt, uint32_t& eq) {
     gt = 0u;
     eq = 0u;
 #pragma unroll
@@ -228,78 +244,24 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
           const uint32_t bin = i0 + q < s1 ? coarse_bin(e4[q]) : 0u;
           const uint32_t bit = 1u << (16 * h + 4 * u + q);
           gt |= bin > b1 ? bit : 0u;
-          if (bin == b1 && i0 + q < s1) {
-            eq |= bit;
-            if (count_sub) atomicAdd(&sm.sub[(e4[q] >> kSubShift) & (kSubBins - 1)], 1u);
-          }
+          eq |= (bin == b1 && i0 + q < s1) ? bit : 0u;
         }
       }
     }
   };
 
-  // ---- 2. the boundary sub-bin sb1: b1's elements by key bits 19..12,
-  //         summed over the cluster; the coarse masks are kept (up to
-  //         kMaskPairs chunk pairs) for the passes below
+  // ---- 2. masks and counts of each thread's elements above b1 (taken
+  //         outright) and in b1 (candidates); the masks of up to kMaskPairs
+  //         chunk pairs are kept for the scatter
   const bool reload = n_chunks > 2;
+  uint32_t n_gt = 0, n_eq = 0;
   for (int c = 0; c < n_chunks; c += 2) {
     if (reload) {
       load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
     }
     uint32_t gt, eq;
-    coarse_masks(c, gt, eq, true);
-    if (c / 2 < kMaskPairs) {
-      sm.mgt[c / 2][t] = gt;
-      sm.meq[c / 2][t] = eq;
-    }
-  }
-  cluster_sync_all();  // #2: every CTA's sub-bin counts are complete
-  {
-    uint32_t sv = 0;  // thread t < 256 holds sub-bin 255 - t (highest first)
-    if (t < kSubBins) {
-      const uint32_t my = smem_u32(&sm.sub[kSubBins - 1 - t]);
-      const uint32_t v0 = ld_cluster_u32(cluster_map(my, 0));
-      const uint32_t v1 = parts > 1 ? ld_cluster_u32(cluster_map(my, 1)) : 0u;
-      const uint32_t v2 = parts > 2 ? ld_cluster_u32(cluster_map(my, 2)) : 0u;
-      const uint32_t v3 = parts > 3 ? ld_cluster_u32(cluster_map(my, 3)) : 0u;
-      sv = v0 + v1 + v2 + v3;
-    }
-    const uint32_t need1 = k - above;
-    const uint32_t ex = block_exclusive_scan(sv, sm.s);
-    if (t < kSubBins && ex < need1 && need1 <= ex + sv) {
-      sm.sb1 = (uint32_t)(kSubBins - 1 - t);
-      sm.above2 = ex;
-    }
-    __syncthreads();
-  }
-  const uint32_t sb1 = sm.sb1;
-  const uint32_t taken = above + sm.above2;  // elements above (b1, sb1)
-
-  // ---- 3a. final masks: an element is taken outright when its (bin, sub-bin)
-  //         is above (b1, sb1), a candidate when equal to it; only b1's few
-  //         elements need their sub-bin, read back from the logits
-  auto final_masks = [&](int c, uint32_t& gt, uint32_t& eq) {
-    if (c / 2 < kMaskPairs) {
-      gt = sm.mgt[c / 2][t];
-      eq = sm.meq[c / 2][t];
-    } else {
-      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
-      coarse_masks(c, gt, eq, false);
-    }
-    uint32_t in = 0u;
-    for (uint32_t m = eq; m != 0u; m &= m - 1u) {
-      const int bit = __ffs(m) - 1;
-      const uint32_t sub = (float_key(__ldca(x + position(c, bit))) >> kSubShift) & (kSubBins - 1);
-      if (sub > sb1) gt |= 1u << bit;
-      else if (sub == sb1) in |= 1u << bit;
-    }
-    eq = in;
-  };
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int c = 0; c < n_chunks; c += 2) {
-    uint32_t gt, eq;
-    final_masks(c, gt, eq);
+    coarse_masks(c, gt, eq);
     n_gt += __popc(gt);
     n_eq += __popc(eq);
     if (c / 2 < kMaskPairs) {
@@ -308,14 +270,14 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
     }
   }
 
-  // ---- 3b. slots: block scan, then the CTAs of the row trade totals
+  // ---- 3. slots: block scan, then the CTAs of the row trade totals
   uint32_t eg, ee, tg, te;
   block_scan2(sm, n_gt, n_eq, eg, ee, tg, te);
   if (t == 0) {
     sm.cta_gt = tg;
     sm.cta_eq = te;
   }
-  cluster_sync_all();  // #3: every CTA's totals are visible
+  cluster_sync_all();  // #2: every CTA's totals are visible
   if (t < 32) {  // lane q reads CTA q's totals, all in flight together
     uint32_t g = 0, e = 0;
     if (t < parts) {
@@ -333,67 +295,103 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   }
   __syncthreads();
 
-  // ---- 3c. elements above (b1, sb1) -> out, its elements -> the leader's list
+  // ---- 4. elements above b1 -> out, b1's elements (key and position) ->
+  //         the leader's candidate list
   const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
   const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
   uint32_t o = sm.o_base + eg;
   uint32_t ce = sm.c_base + ee;
   for (int c = 0; c < n_chunks; c += 2) {
     uint32_t gt, eq;
+    bool in_regs = !reload;  // the pair's keys are in ka / kb
     if (c / 2 < kMaskPairs) {
       gt = sm.mgt[c / 2][t];
       eq = sm.meq[c / 2][t];
     } else {
-      final_masks(c, gt, eq);
+      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      coarse_masks(c, gt, eq);
+      in_regs = true;
     }
     for (; gt != 0u; gt &= gt - 1u) {
-      if (o < taken) out[o] = position(c, __ffs(gt) - 1);
+      if (o < above) out[o] = position(c, __ffs(gt) - 1);
       ++o;
     }
     for (; eq != 0u; eq &= eq - 1u) {
-      const int32_t i = position(c, __ffs(eq) - 1);
+      const int bit = __ffs(eq) - 1;
+      const int32_t i = position(c, bit);
       if (ce < (uint32_t)kCandSmem) {
-        st_cluster_u32(cand_keys0 + 4u * ce, float_key(__ldca(x + i)));
+        const uint32_t key = in_regs ? pair_key(ka, kb, bit) : float_key(__ldca(x + i));
+        st_cluster_u32(cand_keys0 + 4u * ce, key);
         st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)i);
       }
       ++ce;
     }
   }
-  cluster_sync_all();  // #4: the candidates are in the leader; no remote access follows
+  cluster_sync_all();  // #3: the candidates are in the leader; no remote access follows
   if (part != 0) return;
 
-  // ---- 4. the leader takes the remaining k - taken of the candidates, which
-  //         share their top 20 key bits: by rank (key, then position) when
-  //         there are few, else by a radix digit on the low 12 bits
+  // ---- 5. the leader takes the remaining need = k - above of b1's nb
+  //         elements: by their next 8 key bits (sub-bin sb1), then among
+  //         sb1's few elements by rank (key, then position), or by a radix
+  //         digit on the low 12 bits when there are many
   const uint32_t nb = sm.all_eq;
-  const uint32_t need = k - taken;
-  if (nb <= (uint32_t)kSelThreads) {
-    if ((uint32_t)t < nb) {
-      const uint32_t key = sm.cand_keys[t];
-      const int32_t pos = sm.cand_idx[t];
-      uint32_t rank = 0;
-      for (uint32_t q = 0; q < nb; ++q) {
-        const uint32_t kq = sm.cand_keys[q];
-        rank += (kq > key || (kq == key && sm.cand_idx[q] < pos)) ? 1u : 0u;
-      }
-      if (rank < need) out[taken + rank] = pos;
-    }
-    return;
-  }
-  if (t == 0) sm.slot = taken;
-  __syncthreads();
+  const uint32_t need = k - above;
+  if (t == 0) sm.slot = above;
   auto emit = [&](uint32_t, int32_t i) {
     const uint32_t s = warp_claim(&sm.slot, true);
     if (s < k) out[s] = i;
   };
-  const uint32_t prefix = (b1 << kCoarseShift) | (sb1 << kSubShift);
-  if (nb <= (uint32_t)kCandSmem) {
-    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb};
-    radix_select(sm.hist, sm.s, cand, need, prefix, 32 - kSubShift, emit);
-  } else {
+  if (nb > (uint32_t)kCandSmem) {
     // more such elements than the list holds: a radix pass over the row
+    __syncthreads();
     const GlobalLogits<true> row{x, 0, (int64_t)n};
-    radix_select(sm.hist, sm.s, row, need, prefix, 32 - kSubShift, emit);
+    radix_select(sm.hist, sm.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+    return;
+  }
+  for (uint32_t i = t; i < nb; i += kSelThreads)
+    atomicAdd(&sm.sub[(sm.cand_keys[i] >> kSubShift) & (kSubBins - 1)], 1u);
+  __syncthreads();
+  find_threshold_bin(sm.sub, kSubBins, need, sm.s);
+  const uint32_t sb1 = sm.s.bin;
+  const uint32_t above2 = sm.s.above;  // b1's elements above sb1
+  uint32_t* const keys2 = &sm.mgt[0][0];  // sb1's elements (the masks are spent)
+  int32_t* const idx2 = reinterpret_cast<int32_t*>(&sm.meq[0][0]);
+  for (uint32_t i = t; i < nb; i += kSelThreads) {
+    const uint32_t key = sm.cand_keys[i];
+    const int32_t pos = sm.cand_idx[i];
+    const uint32_t sub = (key >> kSubShift) & (kSubBins - 1);
+    const uint32_t s = warp_claim(&sm.slot, sub > sb1);
+    if (sub > sb1 && s < k) out[s] = pos;
+    const uint32_t s2 = warp_claim(&sm.n2, sub == sb1);
+    if (sub == sb1 && s2 < (uint32_t)kList2) {
+      keys2[s2] = key;
+      idx2[s2] = pos;
+    }
+  }
+  __syncthreads();
+  const uint32_t n2 = sm.n2;
+  const uint32_t need2 = need - above2;
+  if (n2 <= (uint32_t)kRankDirect) {
+    if ((uint32_t)t < n2) {
+      const uint32_t key = keys2[t];
+      const int32_t pos = idx2[t];
+      uint32_t rank = 0;
+      for (uint32_t q = 0; q < n2; ++q) {
+        const uint32_t kq = keys2[q];
+        rank += (kq > key || (kq == key && idx2[q] < pos)) ? 1u : 0u;
+      }
+      if (rank < need2) out[above + above2 + rank] = pos;
+    }
+    return;
+  }
+  const uint32_t prefix = (b1 << kCoarseShift) | (sb1 << kSubShift);
+  if (n2 <= (uint32_t)kList2) {
+    const SmemPairs cand{keys2, idx2, (int)n2};
+    radix_select(sm.hist, sm.s, cand, need2, prefix, 32 - kSubShift, emit);
+  } else {
+    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb};
+    radix_select(sm.hist, sm.s, cand, need2, prefix, 32 - kSubShift, emit);
   }
 }
 

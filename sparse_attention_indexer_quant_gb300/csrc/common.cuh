@@ -182,6 +182,12 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+// Atomic add to a shared-memory word of any CTA of the cluster; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_cluster_u32(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
 // Barrier over every thread of every CTA in the cluster; orders the shared
 // memory accesses (local and remote) before it with those after it.
 __device__ __forceinline__ void cluster_sync_all() {

@@ -8,10 +8,10 @@
 //      cluster through distributed shared memory it gives the bin b1 holding
 //      the k-th largest value and the count above it;
 //   2. each thread classifies its elements as above b1 or in it (bit masks);
-//      one block scan and one exchange of CTA totals give every thread its
-//      output and candidate slots; the elements above go straight to the
-//      output, b1's elements (a few hundred for smooth rows) with their keys
-//      into the cluster leader's shared memory;
+//      a warp takes its output and candidate slots with one atomic add per
+//      list on the leader's counters (through distributed shared memory); the
+//      elements above go straight to the output, b1's elements (a few hundred
+//      for smooth rows) with their keys into the leader's shared memory;
 //   3. the leader takes the remaining ones from the candidates: by their next
 //      8 key bits (the sub-bin holding the k-th largest), then among that
 //      sub-bin's elements by rank (key, then position), or by a radix digit
@@ -38,27 +38,24 @@ constexpr int kMaxParts = 4;                            // CTAs per row at most
 constexpr int kMinSlice = 4096;                         // elements per CTA at least
 constexpr int kSubShift = 12;                           // sub-bin: key bits 19..12
 constexpr int kSubBins = 256;
-constexpr int kMaskPairs = 8;                           // chunk pairs whose masks are kept
-constexpr int kList2 = kMaskPairs * kSelThreads;        // boundary sub-bin list (the mask space)
+constexpr int kList2 = 2048;                            // boundary sub-bin list (leader)
 constexpr int kRankDirect = 64;                         // sub-bin lists ranked element by element
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
+static_assert(kSubBins == 8 * 32, "one warp resolves the sub-bin, eight bins a lane");
 
 struct SelSmem {
   uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
-  uint32_t row_bins[kCoarseBins];  // ... and of the row (sum over the cluster)
-  uint32_t sub[kSubBins];      // this CTA's b1 elements by the next 8 key bits
-  uint32_t mgt[kMaskPairs][kSelThreads];  // per thread and chunk pair: taken outright
-  uint32_t meq[kMaskPairs][kSelThreads];  // ... and boundary candidates
-  uint32_t n2;                 // candidates in the boundary sub-bin (leader)
+  uint32_t sub[kSubBins];      // the candidates by their next 8 key bits (leader)
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
-  uint32_t warp_gt[kSelThreads / 32], warp_eq[kSelThreads / 32];
-  uint32_t cta_gt, cta_eq;     // this CTA's counts above / in b1 (read by the cluster)
-  uint32_t o_base, c_base;     // this CTA's first output / candidate slot
-  uint32_t all_eq;             // the row's elements in b1
-  uint32_t slot;               // next output slot of the exact pass
+  uint32_t nb1;                // the row's elements in the boundary bin
+  uint32_t n_out;              // output slots handed out (leader; the cluster adds to it)
+  uint32_t n_cand;             // candidate slots handed out (leader; likewise)
+  uint32_t n2;                 // candidates in the boundary sub-bin (leader)
   uint32_t cand_keys[kCandSmem];
   int32_t cand_idx[kCandSmem];
+  uint32_t keys2[kList2];      // the boundary sub-bin's candidates (leader)
+  int32_t idx2[kList2];
 };
 
 // Keys of x[i] for this thread's 16 positions of the chunk at `base`
@@ -110,49 +107,46 @@ __device__ __forceinline__ void hist_keys(uint32_t* bins, const uint4 (&kv)[kSel
   }
 }
 
-// Exclusive prefix sums of a and b over the block's threads (ea, eb) and their
-// block totals (ta, tb).  The caller syncs before the scratch is reused.
-__device__ __forceinline__ void block_scan2(SelSmem& sm, uint32_t a, uint32_t b, uint32_t& ea,
-                                            uint32_t& eb, uint32_t& ta, uint32_t& tb) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t xa = a, xb = b;
+// In warp 0 of the block: the bin b of hist[0, kSubBins) with
+// count(bins > b) < need <= count(bins >= b) -> sc.bin, and count(bins > b)
+// -> sc.above.  Requires 1 <= need <= the total count.
+__device__ __forceinline__ void warp_find_sub_bin(const uint32_t* hist, uint32_t need,
+                                                  ScanScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h[8], local = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {  // bins kSubBins - 1 - 8 * lane - q, highest first
+    h[q] = hist[kSubBins - 1 - 8 * lane - q];
+    local += h[q];
+  }
+  uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t ya = __shfl_up_sync(0xFFFFFFFFu, xa, o);
-    const uint32_t yb = __shfl_up_sync(0xFFFFFFFFu, xb, o);
-    if (lane >= o) {
-      xa += ya;
-      xb += yb;
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t run = incl - local;
+  if (run < need && need <= incl) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run < need && need <= run + h[q]) {
+        sc.bin = (uint32_t)(kSubBins - 1 - 8 * lane - q);
+        sc.above = run;
+      }
+      run += h[q];
     }
   }
-  if (lane == 31) {
-    sm.warp_gt[warp] = xa;
-    sm.warp_eq[warp] = xb;
-  }
-  __syncthreads();
-  uint32_t pa = 0, pb = 0, sa = 0, sb = 0;
-#pragma unroll
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    const uint32_t va = sm.warp_gt[w], vb = sm.warp_eq[w];
-    pa += w < warp ? va : 0u;
-    pb += w < warp ? vb : 0u;
-    sa += va;
-    sb += vb;
-  }
-  ea = pa + xa - a;
-  eb = pb + xb - b;
-  ta = sa;
-  tb = sb;
 }
 
 // The k largest of x[0, len) -> out[0, k) (positions, -1 padded).  Called by
 // every thread of every CTA of a cluster of `parts` CTAs (kSelThreads each)
 // with the same arguments; every CTA takes the same branches and passes the
-// same three cluster barriers.
+// same two cluster barriers.
 __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, int64_t len,
                                                    uint32_t k, int32_t* out, int parts) {
   const int part = (int)cluster_ctarank();
   const int t = threadIdx.x;
+  const int lane = t & 31;
   const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   if (len <= (int64_t)k) {  // the whole cluster leaves here
     if (part == 0)
@@ -175,12 +169,15 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   if (t == 0) {
     sm.s.bin = 0;
     sm.s.above = 0;
+    sm.nb1 = 0;
+    sm.n_out = 0;
+    sm.n_cand = 0;
     sm.n2 = 0;
   }
   __syncthreads();
 
   // ---- 1. coarse histogram of the slice, then of the row
-  for (int c = 0; c < n_chunks; c += 2) {  // (past two chunks the later passes reload)
+  for (int c = 0; c < n_chunks; c += 2) {  // (past two chunks the later pass reloads)
     if (c > 0) {
       load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
       load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
@@ -188,10 +185,10 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
     hist_keys(sm.bins, ka, s0 + c * kSelChunk, s1, t);
     hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
   }
-  cluster_sync_all();  // #1: every CTA's slice histogram is complete
-  // thread t's bins 4095 - 8t down to 4088 - 8t, summed over the cluster (all
-  // of a thread's remote loads are issued before any is used)
-  uint32_t local = 0;
+  cluster_sync_all();  // #1: every CTA's slice histogram is complete, the counters zeroed
+  // thread t's bins 4088 - 8t + j (j = 0..7), summed over the cluster (all of
+  // a thread's remote loads are issued before any is used)
+  uint32_t h8[8], local = 0;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {  // 4 bins at a time
     const uint32_t my = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t + 4 * half]);
@@ -200,19 +197,23 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
     const uint4 v1 = parts > 1 ? ld_cluster_v4(cluster_map(my, 1)) : z;
     const uint4 v2 = parts > 2 ? ld_cluster_v4(cluster_map(my, 2)) : z;
     const uint4 v3 = parts > 3 ? ld_cluster_v4(cluster_map(my, 3)) : z;
-    const uint4 acc = make_uint4(v0.x + v1.x + v2.x + v3.x, v0.y + v1.y + v2.y + v3.y,
-                                 v0.z + v1.z + v2.z + v3.z, v0.w + v1.w + v2.w + v3.w);
-    *reinterpret_cast<uint4*>(&sm.row_bins[kCoarseBins - 8 - 8 * t + 4 * half]) = acc;
-    local += acc.x + acc.y + acc.z + acc.w;
+    h8[4 * half + 0] = v0.x + v1.x + v2.x + v3.x;
+    h8[4 * half + 1] = v0.y + v1.y + v2.y + v3.y;
+    h8[4 * half + 2] = v0.z + v1.z + v2.z + v3.z;
+    h8[4 * half + 3] = v0.w + v1.w + v2.w + v3.w;
   }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) local += h8[j];
   const uint32_t excl = block_exclusive_scan(local, sm.s);
   if (excl < k && k <= excl + local) {
     uint32_t run = excl;
+#pragma unroll
     for (int q = 0; q < 8; ++q) {  // bins 4095 - 8t - q, highest first
-      const uint32_t h = sm.row_bins[kCoarseBins - 1 - 8 * t - q];
+      const uint32_t h = h8[7 - q];
       if (run < k && k <= run + h) {
         sm.s.bin = (uint32_t)(kCoarseBins - 1 - 8 * t - q);
         sm.s.above = run;
+        sm.nb1 = h;
       }
       run += h;
     }
@@ -220,18 +221,30 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   __syncthreads();
   const uint32_t b1 = sm.s.bin;
   const uint32_t above = sm.s.above;  // the row's elements in bins above b1
+  const uint32_t nb = sm.nb1;         // ... and in b1
 
   // Each thread's elements of a chunk pair are 32 mask bits: bit 16*h + 4*u + q
   // is chunk h of the pair, float4 u, lane q of it.
   auto position = [&](int c, int bit) -> int32_t {  // chunk pair starting at chunk c
     return s0 + (c + (bit >> 4)) * kSelChunk + 4 * (((bit >> 2) & 3) * kSelThreads + t) + (bit & 3);
   };
-  // masks of the elements above b1 and in b1 (positions past the slice are
-  // skipped: their key(-inf) padding is in b1 when the row's k-th largest
-  // value is itself -inf)
-  auto coarse_masks = [&](int c, uint32_t& gt, uint32_t& eq) {
-    gt = 0u;
-    eq = 0u;
+
+  // ---- 2. each thread's elements above b1 go to the output, those in b1
+  //         (key and position) to the leader's candidate list; a warp takes
+  //         its slots with one atomic add per list on the leader's counters
+  //         (positions past the slice are skipped: their key(-inf) padding is
+  //         in b1 when the row's k-th largest value is itself -inf)
+  const uint32_t n_out0 = cluster_map(smem_u32(&sm.n_out), 0);
+  const uint32_t n_cand0 = cluster_map(smem_u32(&sm.n_cand), 0);
+  const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
+  const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
+  const bool reload = n_chunks > 2;
+  for (int c = 0; c < n_chunks; c += 2) {
+    if (reload) {
+      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
+      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
+    }
+    uint32_t gt = 0u, eq = 0u;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -248,103 +261,52 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
         }
       }
     }
-  };
-
-  // ---- 2. masks and counts of each thread's elements above b1 (taken
-  //         outright) and in b1 (candidates); the masks of up to kMaskPairs
-  //         chunk pairs are kept for the scatter
-  const bool reload = n_chunks > 2;
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int c = 0; c < n_chunks; c += 2) {
-    if (reload) {
-      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
+    const uint32_t ng = __popc(gt), ne = __popc(eq);
+    uint32_t ig = ng, ie = ne;  // inclusive sums over the warp's lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
+      const uint32_t ye = __shfl_up_sync(0xFFFFFFFFu, ie, o);
+      if (lane >= o) {
+        ig += yg;
+        ie += ye;
+      }
     }
-    uint32_t gt, eq;
-    coarse_masks(c, gt, eq);
-    n_gt += __popc(gt);
-    n_eq += __popc(eq);
-    if (c / 2 < kMaskPairs) {
-      sm.mgt[c / 2][t] = gt;
-      sm.meq[c / 2][t] = eq;
+    uint32_t bg = 0, be = 0;
+    if (lane == 31) {  // the warp's totals
+      if (ig != 0u) bg = atom_add_cluster_u32(n_out0, ig);
+      if (ie != 0u) be = atom_add_cluster_u32(n_cand0, ie);
     }
-  }
-
-  // ---- 3. slots: block scan, then the CTAs of the row trade totals
-  uint32_t eg, ee, tg, te;
-  block_scan2(sm, n_gt, n_eq, eg, ee, tg, te);
-  if (t == 0) {
-    sm.cta_gt = tg;
-    sm.cta_eq = te;
-  }
-  cluster_sync_all();  // #2: every CTA's totals are visible
-  if (t < 32) {  // lane q reads CTA q's totals, all in flight together
-    uint32_t g = 0, e = 0;
-    if (t < parts) {
-      g = ld_cluster_u32(cluster_map(smem_u32(&sm.cta_gt), t));
-      e = ld_cluster_u32(cluster_map(smem_u32(&sm.cta_eq), t));
-    }
-    const uint32_t bg = __reduce_add_sync(0xFFFFFFFFu, t < part ? g : 0u);
-    const uint32_t be = __reduce_add_sync(0xFFFFFFFFu, t < part ? e : 0u);
-    const uint32_t ae = __reduce_add_sync(0xFFFFFFFFu, e);
-    if (t == 0) {
-      sm.o_base = bg;
-      sm.c_base = be;
-      sm.all_eq = ae;
-    }
-  }
-  __syncthreads();
-
-  // ---- 4. elements above b1 -> out, b1's elements (key and position) ->
-  //         the leader's candidate list
-  const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
-  const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
-  uint32_t o = sm.o_base + eg;
-  uint32_t ce = sm.c_base + ee;
-  for (int c = 0; c < n_chunks; c += 2) {
-    uint32_t gt, eq;
-    bool in_regs = !reload;  // the pair's keys are in ka / kb
-    if (c / 2 < kMaskPairs) {
-      gt = sm.mgt[c / 2][t];
-      eq = sm.meq[c / 2][t];
-    } else {
-      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
-      coarse_masks(c, gt, eq);
-      in_regs = true;
-    }
+    uint32_t o = __shfl_sync(0xFFFFFFFFu, bg, 31) + ig - ng;
+    uint32_t ce = __shfl_sync(0xFFFFFFFFu, be, 31) + ie - ne;
     for (; gt != 0u; gt &= gt - 1u) {
       if (o < above) out[o] = position(c, __ffs(gt) - 1);
       ++o;
     }
     for (; eq != 0u; eq &= eq - 1u) {
       const int bit = __ffs(eq) - 1;
-      const int32_t i = position(c, bit);
       if (ce < (uint32_t)kCandSmem) {
-        const uint32_t key = in_regs ? pair_key(ka, kb, bit) : float_key(__ldca(x + i));
-        st_cluster_u32(cand_keys0 + 4u * ce, key);
-        st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)i);
+        st_cluster_u32(cand_keys0 + 4u * ce, pair_key(ka, kb, bit));
+        st_cluster_u32(cand_idx0 + 4u * ce, (uint32_t)position(c, bit));
       }
       ++ce;
     }
   }
-  cluster_sync_all();  // #3: the candidates are in the leader; no remote access follows
+  cluster_sync_all();  // #2: the candidates are in the leader; no remote access follows
   if (part != 0) return;
 
-  // ---- 5. the leader takes the remaining need = k - above of b1's nb
+  // ---- 3. the leader takes the remaining need = k - above of b1's nb
   //         elements: by their next 8 key bits (sub-bin sb1), then among
   //         sb1's few elements by rank (key, then position), or by a radix
-  //         digit on the low 12 bits when there are many
-  const uint32_t nb = sm.all_eq;
+  //         digit on the low 12 bits when there are many.  Its output
+  //         counter stands at `above` and hands out the remaining slots.
   const uint32_t need = k - above;
-  if (t == 0) sm.slot = above;
   auto emit = [&](uint32_t, int32_t i) {
-    const uint32_t s = warp_claim(&sm.slot, true);
+    const uint32_t s = warp_claim(&sm.n_out, true);
     if (s < k) out[s] = i;
   };
   if (nb > (uint32_t)kCandSmem) {
-    // more such elements than the list holds: a radix pass over the row
-    __syncthreads();
+    // more such elements than the list holds: radix passes over the row
     const GlobalLogits<true> row{x, 0, (int64_t)n};
     radix_select(sm.hist, sm.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
     return;
@@ -352,21 +314,20 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   for (uint32_t i = t; i < nb; i += kSelThreads)
     atomicAdd(&sm.sub[(sm.cand_keys[i] >> kSubShift) & (kSubBins - 1)], 1u);
   __syncthreads();
-  find_threshold_bin(sm.sub, kSubBins, need, sm.s);
+  if (t < 32) warp_find_sub_bin(sm.sub, need, sm.s);
+  __syncthreads();
   const uint32_t sb1 = sm.s.bin;
   const uint32_t above2 = sm.s.above;  // b1's elements above sb1
-  uint32_t* const keys2 = &sm.mgt[0][0];  // sb1's elements (the masks are spent)
-  int32_t* const idx2 = reinterpret_cast<int32_t*>(&sm.meq[0][0]);
   for (uint32_t i = t; i < nb; i += kSelThreads) {
     const uint32_t key = sm.cand_keys[i];
     const int32_t pos = sm.cand_idx[i];
     const uint32_t sub = (key >> kSubShift) & (kSubBins - 1);
-    const uint32_t s = warp_claim(&sm.slot, sub > sb1);
+    const uint32_t s = warp_claim(&sm.n_out, sub > sb1);
     if (sub > sb1 && s < k) out[s] = pos;
     const uint32_t s2 = warp_claim(&sm.n2, sub == sb1);
     if (sub == sb1 && s2 < (uint32_t)kList2) {
-      keys2[s2] = key;
-      idx2[s2] = pos;
+      sm.keys2[s2] = key;
+      sm.idx2[s2] = pos;
     }
   }
   __syncthreads();
@@ -374,12 +335,12 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   const uint32_t need2 = need - above2;
   if (n2 <= (uint32_t)kRankDirect) {
     if ((uint32_t)t < n2) {
-      const uint32_t key = keys2[t];
-      const int32_t pos = idx2[t];
+      const uint32_t key = sm.keys2[t];
+      const int32_t pos = sm.idx2[t];
       uint32_t rank = 0;
       for (uint32_t q = 0; q < n2; ++q) {
-        const uint32_t kq = keys2[q];
-        rank += (kq > key || (kq == key && idx2[q] < pos)) ? 1u : 0u;
+        const uint32_t kq = sm.keys2[q];
+        rank += (kq > key || (kq == key && sm.idx2[q] < pos)) ? 1u : 0u;
       }
       if (rank < need2) out[above + above2 + rank] = pos;
     }
@@ -387,7 +348,7 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   }
   const uint32_t prefix = (b1 << kCoarseShift) | (sb1 << kSubShift);
   if (n2 <= (uint32_t)kList2) {
-    const SmemPairs cand{keys2, idx2, (int)n2};
+    const SmemPairs cand{sm.keys2, sm.idx2, (int)n2};
     radix_select(sm.hist, sm.s, cand, need2, prefix, 32 - kSubShift, emit);
   } else {
     const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb};

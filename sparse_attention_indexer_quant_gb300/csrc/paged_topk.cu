@@ -10,7 +10,7 @@
 //   3. select   one thread-block cluster of P CTAs per row running
 //               cluster_select_row (select_row.cuh) over the row's logits.
 // All three are dependent launches, so each one's start overlaps the previous
-// one's tail.
+// one's tail (the zero kernel's only after every earlier kernel is done).
 //
 // Workspace (device, caller-owned), 256-byte aligned pieces: the u32 work-item
 // counter (zeroed per call), then f32 logits [rows][ldw], ldw = max_blocks * 64.
@@ -52,12 +52,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
                                                                       int parts) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  pdl_wait();  // the scoring pass's logits
   const int64_t rows = (int64_t)p.B * next_n;
   const TopkWs ws = ws_layout(p.workspace, rows, p.max_blocks, nullptr);
   const int64_t r = blockIdx.x / parts;
   const int b = (int)(r / next_n), j = (int)(r % next_n);
+  // an input of the call, read before the wait: this launch can only have
+  // started after the zero kernel's wait, i.e. after every kernel issued
+  // before the call completed
   int64_t L = __ldg(p.context_lens + b);
+  pdl_wait();  // the scoring pass's logits
   const int64_t cap = (int64_t)p.max_blocks * kPage;
   L = L < 0 ? 0 : (L > cap ? cap : L);
   int64_t len = L - next_n + j + 1;
@@ -67,11 +70,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
                      parts);
 }
 
-// Zeroes the scoring pass's work-item counter.
+// Zeroes the scoring pass's work-item counter.  It waits for every earlier
+// kernel (the previous call's are done with the workspace) before it lets
+// the scoring pass start, so the kernels after it may read the call's inputs
+// before their own waits.
 __global__ void __launch_bounds__(32) paged_ws_zero_kernel(uint32_t* counter) {
-  pdl_launch_dependents();
-  pdl_wait();  // the previous call's kernels are done with the workspace
+  pdl_wait();
   if (threadIdx.x == 0) *counter = 0u;
+  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -58,25 +58,32 @@ struct SelSmem {
   int32_t idx2[kList2];
 };
 
-// Keys of x[i] for this thread's 16 positions of the chunk at `base`
-// (key(-inf) at positions from s1 on, which the passes below never count).
-// Four at a time when x is 16-byte aligned (base is a multiple of 4), else
-// one by one.
-__device__ __forceinline__ void load_chunk_keys(const float* x, bool aligned, int32_t base,
-                                                int32_t s1, int t, uint4 (&kv)[kSelVec]) {
+// Keys of x[i] for this thread's 32 positions of the chunk pair at `base`
+// (chunks base and base + kSelChunk; key(-inf) at positions from s1 on, which
+// the passes below never count).  Four at a time when x is 16-byte aligned
+// (base is a multiple of 4), else one by one; all of a thread's loads are
+// issued before any key is formed, so they are in flight together.
+__device__ __forceinline__ void load_pair_keys(const float* x, bool aligned, int32_t base,
+                                               int32_t s1, int t, uint4 (&ka)[kSelVec],
+                                               uint4 (&kb)[kSelVec]) {
+  float4 v[2 * kSelVec];
+#pragma unroll
+  for (int j = 0; j < 2 * kSelVec; ++j) {
+    const int32_t i0 = base + (j / kSelVec) * kSelChunk + 4 * ((j % kSelVec) * kSelThreads + t);
+    if (aligned && i0 + 3 < s1) {
+      v[j] = __ldca(reinterpret_cast<const float4*>(x + i0));
+    } else {
+      v[j].x = i0 + 0 < s1 ? __ldca(x + i0 + 0) : -INFINITY;
+      v[j].y = i0 + 1 < s1 ? __ldca(x + i0 + 1) : -INFINITY;
+      v[j].z = i0 + 2 < s1 ? __ldca(x + i0 + 2) : -INFINITY;
+      v[j].w = i0 + 3 < s1 ? __ldca(x + i0 + 3) : -INFINITY;
+    }
+  }
 #pragma unroll
   for (int u = 0; u < kSelVec; ++u) {
-    const int32_t i0 = base + 4 * (u * kSelThreads + t);
-    float4 v;
-    if (aligned && i0 + 3 < s1) {
-      v = __ldca(reinterpret_cast<const float4*>(x + i0));
-    } else {
-      v.x = i0 + 0 < s1 ? __ldca(x + i0 + 0) : -INFINITY;
-      v.y = i0 + 1 < s1 ? __ldca(x + i0 + 1) : -INFINITY;
-      v.z = i0 + 2 < s1 ? __ldca(x + i0 + 2) : -INFINITY;
-      v.w = i0 + 3 < s1 ? __ldca(x + i0 + 3) : -INFINITY;
-    }
-    kv[u] = make_uint4(float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w));
+    const float4 a = v[u], b = v[kSelVec + u];
+    ka[u] = make_uint4(float_key(a.x), float_key(a.y), float_key(a.z), float_key(a.w));
+    kb[u] = make_uint4(float_key(b.x), float_key(b.y), float_key(b.z), float_key(b.w));
   }
 }
 
@@ -161,8 +168,7 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   const int n_chunks = (slice + kSelChunk - 1) / kSelChunk;
 
   uint4 ka[kSelVec], kb[kSelVec];
-  load_chunk_keys(x, aligned, s0, s1, t, ka);
-  load_chunk_keys(x, aligned, s0 + kSelChunk, s1, t, kb);
+  load_pair_keys(x, aligned, s0, s1, t, ka, kb);
 #pragma unroll
   for (int q = 0; q < 8; ++q) sm.bins[8 * t + q] = 0u;
   if (t < kSubBins) sm.sub[t] = 0u;
@@ -179,8 +185,7 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   // ---- 1. coarse histogram of the slice, then of the row
   for (int c = 0; c < n_chunks; c += 2) {  // (past two chunks the later pass reloads)
     if (c > 0) {
-      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      load_pair_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka, kb);
     }
     hist_keys(sm.bins, ka, s0 + c * kSelChunk, s1, t);
     hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
@@ -189,18 +194,31 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   // thread t's bins 4088 - 8t + j (j = 0..7), summed over the cluster (all of
   // a thread's remote loads are issued before any is used)
   uint32_t h8[8], local = 0;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {  // 4 bins at a time
-    const uint32_t my = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t + 4 * half]);
+  {
+    const uint32_t my0 = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t]);
+    const uint32_t my1 = my0 + 16u;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 v0 = ld_cluster_v4(cluster_map(my, 0));
-    const uint4 v1 = parts > 1 ? ld_cluster_v4(cluster_map(my, 1)) : z;
-    const uint4 v2 = parts > 2 ? ld_cluster_v4(cluster_map(my, 2)) : z;
-    const uint4 v3 = parts > 3 ? ld_cluster_v4(cluster_map(my, 3)) : z;
-    h8[4 * half + 0] = v0.x + v1.x + v2.x + v3.x;
-    h8[4 * half + 1] = v0.y + v1.y + v2.y + v3.y;
-    h8[4 * half + 2] = v0.z + v1.z + v2.z + v3.z;
-    h8[4 * half + 3] = v0.w + v1.w + v2.w + v3.w;
+    uint4 v[2 * kMaxParts];
+#pragma unroll
+    for (int q = 0; q < kMaxParts; ++q) {
+      v[2 * q] = q < parts ? ld_cluster_v4(cluster_map(my0, q)) : z;
+      v[2 * q + 1] = q < parts ? ld_cluster_v4(cluster_map(my1, q)) : z;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 a = v[half];
+#pragma unroll
+      for (int q = 1; q < kMaxParts; ++q) {
+        a.x += v[2 * q + half].x;
+        a.y += v[2 * q + half].y;
+        a.z += v[2 * q + half].z;
+        a.w += v[2 * q + half].w;
+      }
+      h8[4 * half + 0] = a.x;
+      h8[4 * half + 1] = a.y;
+      h8[4 * half + 2] = a.z;
+      h8[4 * half + 3] = a.w;
+    }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) local += h8[j];
@@ -241,8 +259,7 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   const bool reload = n_chunks > 2;
   for (int c = 0; c < n_chunks; c += 2) {
     if (reload) {
-      load_chunk_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka);
-      load_chunk_keys(x, aligned, s0 + (c + 1) * kSelChunk, s1, t, kb);
+      load_pair_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka, kb);
     }
     uint32_t gt = 0u, eq = 0u;
 #pragma unroll

@@ -108,9 +108,14 @@ __device__ __forceinline__ void hist_keys(uint32_t* bins, const uint4 (&kv)[kSel
   for (int u = 0; u < kSelVec; ++u) {
     const int32_t i0 = base + 4 * (u * kSelThreads + t);
     const uint32_t e4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+    if (i0 + 3 < s1) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (i0 + q < s1) atomicAdd(&bins[coarse_bin(e4[q])], 1u);
+      for (int q = 0; q < 4; ++q) atomicAdd(&bins[coarse_bin(e4[q])], 1u);
+    } else if (i0 < s1) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q < s1) atomicAdd(&bins[coarse_bin(e4[q])], 1u);
+    }
   }
 }
 
@@ -256,25 +261,45 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
   const uint32_t n_cand0 = cluster_map(smem_u32(&sm.n_cand), 0);
   const uint32_t cand_keys0 = cluster_map(smem_u32(sm.cand_keys), 0);
   const uint32_t cand_idx0 = cluster_map(smem_u32(sm.cand_idx), 0);
+  const uint32_t key_b1 = b1 << kCoarseShift;                  // b1's keys share these top bits
+  const uint32_t key_gt = key_b1 | ((1u << kCoarseShift) - 1u);  // keys above b1 exceed this
+  const uint32_t pad_bin = coarse_bin(float_key(-INFINITY));   // the padding's bin
   const bool reload = n_chunks > 2;
   for (int c = 0; c < n_chunks; c += 2) {
     if (reload) {
       load_pair_keys(x, aligned, s0 + c * kSelChunk, s1, t, ka, kb);
     }
     uint32_t gt = 0u, eq = 0u;
+    if (b1 > pad_bin) {  // the key(-inf) padding is neither above b1 nor in it
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int u = 0; u < kSelVec; ++u) {
-        const uint4 v = h == 0 ? ka[u] : kb[u];
-        const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
-        const int32_t i0 = s0 + (c + h) * kSelChunk + 4 * (u * kSelThreads + t);
+        for (int u = 0; u < kSelVec; ++u) {
+          const uint4 v = h == 0 ? ka[u] : kb[u];
+          const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t bin = i0 + q < s1 ? coarse_bin(e4[q]) : 0u;
-          const uint32_t bit = 1u << (16 * h + 4 * u + q);
-          gt |= bin > b1 ? bit : 0u;
-          eq |= (bin == b1 && i0 + q < s1) ? bit : 0u;
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t bit = 1u << (16 * h + 4 * u + q);
+            gt |= e4[q] > key_gt ? bit : 0u;
+            eq |= (e4[q] ^ key_b1) < (1u << kCoarseShift) ? bit : 0u;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int u = 0; u < kSelVec; ++u) {
+          const uint4 v = h == 0 ? ka[u] : kb[u];
+          const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
+          const int32_t i0 = s0 + (c + h) * kSelChunk + 4 * (u * kSelThreads + t);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t bit = 1u << (16 * h + 4 * u + q);
+            const bool in = i0 + q < s1;
+            gt |= (e4[q] > key_gt && in) ? bit : 0u;
+            eq |= ((e4[q] ^ key_b1) < (1u << kCoarseShift) && in) ? bit : 0u;
+          }
         }
       }
     }

@@ -187,6 +187,8 @@ IDX_API idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld,
  *                    aligned; its contents need no initialisation and are
  *                    meaningless after the call.  Calls that share a workspace
  *                    must not overlap on the GPU.
+ *   A batch of more than about 16 million work items (B times the items per
+ *   sequence, up to 16 pages each) is rejected with IDX_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------ */
 IDX_API size_t idx_paged_logits_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks,
                                              int32_t page_size, int32_t k);
@@ -215,7 +217,8 @@ IDX_API idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q
  *   rejected with IDX_ERR_INVALID_ARG (and a message on stderr); use
  *   idx_paged_logits_topk with a caller workspace for it.
  *   All calls share the one scratch array: calls that overlap on the GPU race.
- *   Every call clears the parts that must start at zero.
+ *   Nothing in the scratch needs clearing between calls: its work-item
+ *   counter carries each call's generation.
  * ------------------------------------------------------------------------ */
 IDX_API idx_status idx_paged_logits_topk_noalloc(
     const uint8_t* q_vals, const uint8_t* q_scales, int32_t B, int32_t next_n, int32_t H,

@@ -33,6 +33,16 @@ idx_status ok() {
   return IDX_OK;
 }
 
+// Generations of the fused call's work-item counter: distinct per call (of the
+// process), nonzero (a zero-filled workspace matches no call), below 2^40.
+unsigned long long next_item_generation() {
+  static std::atomic<unsigned long long> g_next{1};
+  constexpr unsigned long long kMask = (1ull << (64 - idx::kItemBits)) - 1ull;
+  unsigned long long g = g_next.fetch_add(1) & kMask;
+  while (g == 0) g = g_next.fetch_add(1) & kMask;
+  return g;
+}
+
 idx_status from_cuda(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return ok();
   return fail(IDX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -340,6 +350,12 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
       B, max_blocks, (int64_t)sms * idx::paged_ctas_per_sm(H * next_n));
   set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n, item_tiles);
   if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks too large");
+  // every claim of the call (items, plus one failing and one stale claim per
+  // CTA) must fit the counter's item field
+  if ((int64_t)B * a.chunks + 2 * (int64_t)a.grid >= (int64_t(1) << idx::kItemBits) - 1)
+    return fail(IDX_ERR_INVALID_ARG, "B * work items per sequence = %lld too large",
+                (long long)B * a.chunks);
+  a.item_gen = next_item_generation();
   a.topk = k;
   a.out_idx = out_idx;
   a.workspace = workspace;

@@ -37,7 +37,11 @@ struct PagedArgs {
   int32_t topk;           // fused only
   int32_t* out_idx;       // fused only: [rows, topk]
   void* workspace;        // fused only
-  uint32_t* item_counter; // zeroed work-item counter: dynamic scheduling; null: static
+  unsigned long long* item_counter;  // generation-tagged work-item counter: dynamic
+                                     // scheduling; null: static
+  unsigned long long item_gen;       // this call's generation (nonzero, < 2^40)
+  int32_t wait_first;                // wait for the previous kernel before letting the
+                                     // next one start (its early code may read the inputs)
   idx_device_errors* errors;
 };
 

@@ -142,6 +142,42 @@ __device__ __forceinline__ uint8_t* aligned_smem_base() {
   return smem_raw + ((1024u - (a & 1023u)) & 1023u);
 }
 
+// Work-item counter of the dynamic schedule, kept in a workspace that calls
+// reuse: the top 40 bits hold the call's generation, the low kItemBits the
+// items handed out.  A call's first claim finds an older generation's value
+// (or whatever a fresh workspace held) and installs its own, so the counter
+// needs no clearing between calls.  Returns the call's next item index;
+// 0xFFFFFFFF (past every item) if the installing race does not settle.
+constexpr int kItemBits = 24;
+__device__ __forceinline__ uint32_t claim_item(unsigned long long* ctr, unsigned long long gen,
+                                               idx_device_errors* errors) {
+  constexpr unsigned long long kCount = (1ull << kItemBits) - 1ull;
+  unsigned long long v = atomicAdd(ctr, 1ull);
+  if ((v >> kItemBits) == gen) return (uint32_t)(v & kCount);
+  unsigned long long cur = v + 1ull;  // the stale value, as this thread left it
+  for (int i = 0; i < (1 << 16); ++i) {
+    const unsigned long long prev = atomicCAS(ctr, cur, (gen << kItemBits) | 1ull);
+    if (prev == cur) return 0u;  // installed, with item 0 claimed
+    if ((prev >> kItemBits) == gen) return (uint32_t)(atomicAdd(ctr, 1ull) & kCount);
+    cur = prev;  // other claims moved the stale value on
+  }
+  flag_timeout(errors, kTimeoutProducer);
+  return 0xFFFFFFFFu;
+}
+
+// Installs this call's generation in the counter ahead of the first claims
+// (one thread of the grid, while its warp has nothing else to do yet), so
+// that the claims find it in place and take one atomic add each; claims that
+// come first install it themselves.
+__device__ __forceinline__ void install_generation(unsigned long long* ctr, unsigned long long gen) {
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int i = 0; i < 64 && (cur >> kItemBits) != gen; ++i) {
+    const unsigned long long prev = atomicCAS(ctr, cur, gen << kItemBits);
+    if (prev == cur) return;
+    cur = prev;
+  }
+}
+
 // Barrier among the four epilogue warps only.
 __device__ __forceinline__ void epilogue_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
@@ -150,7 +186,7 @@ __device__ __forceinline__ void epilogue_sync() {
 template <int H, int NEXT_N, class Ep>
 __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const uint8_t* kcache,
                                                      bool dynamic, bool pass_empty,
-                                                     uint32_t* item_counter) {
+                                                     unsigned long long* item_counter) {
   constexpr int NH = H * NEXT_N;
   using Lay = PagedLayout<NH>;
   constexpr int ACC = Lay::kAccBufs;
@@ -204,8 +240,13 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   // up to here only this CTA's shared and tensor memory was touched: with a
   // dependent launch that overlaps the previous kernel's tail; every input is
   // read after the wait
-  pdl_launch_dependents();
-  pdl_wait();
+  if (p.wait_first) {
+    pdl_wait();
+    pdl_launch_dependents();
+  } else {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
   for (int i = threadIdx.x; i < p.B && i < kClCache; i += kPagedThreads)
     sCl[i] = __ldg(p.context_lens + i);
   Ep::init(extra);
@@ -214,6 +255,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int64_t n_items = (int64_t)p.B * p.chunks;
+  if (dynamic && blockIdx.x == 0 && threadIdx.x == 0) install_generation(item_counter, p.item_gen);
 
   if (warp == 5) {
     // ---------------------------------------------------------- item loader
@@ -229,7 +271,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
       while (true) {
         if (dynamic && !first) {
           uint32_t t = 0;
-          if (lane == 0) t = atomicAdd(item_counter, 1u);
+          if (lane == 0) t = claim_item(item_counter, p.item_gen, p.errors);
           w = (int64_t)gridDim.x + (int64_t)__shfl_sync(kAll, t, 0);
         } else {
           w += gridDim.x;

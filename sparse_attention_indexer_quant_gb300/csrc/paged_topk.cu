@@ -3,17 +3,18 @@
 // launches that hand the logits over through the caller's workspace instead of
 // a logits tensor:
 //
-//   1. zero     the scoring pass's work-item counter;
-//   2. score    the persistent cp.async + tcgen05 logits kernel, taking work items
-//               from the counter and writing each row's valid logits to a
-//               row-major scratch that stays in L2 for these sizes;
-//   3. select   one thread-block cluster of P CTAs per row running
+//   1. score    the persistent cp.async + tcgen05 logits kernel, taking work items
+//               from a generation-tagged counter and writing each row's valid
+//               logits to a row-major scratch that stays in L2 for these sizes;
+//   2. select   one thread-block cluster of P CTAs per row running
 //               cluster_select_row (select_row.cuh) over the row's logits.
-// All three are dependent launches, so each one's start overlaps the previous
-// one's tail (the zero kernel's only after every earlier kernel is done).
+// Both are dependent launches.  The scoring pass lets the select launch start
+// only once every earlier kernel is done, so the select reads the call's
+// inputs before waiting for the logits.
 //
-// Workspace (device, caller-owned), 256-byte aligned pieces: the u32 work-item
-// counter (zeroed per call), then f32 logits [rows][ldw], ldw = max_blocks * 64.
+// Workspace (device, caller-owned), 256-byte aligned pieces: the u64 work-item
+// counter (no clearing needed: see claim_item), then f32 logits [rows][ldw],
+// ldw = max_blocks * 64.
 #include <math.h>
 
 #include "common.cuh"
@@ -25,10 +26,9 @@ namespace idx {
 namespace {
 
 struct TopkWs {
-  uint32_t* items;    // work-item counter of the scoring pass
-  float* logits;      // [rows][ldw]
+  unsigned long long* items;  // work-item counter of the scoring pass
+  float* logits;              // [rows][ldw]
   int64_t ldw;
-  size_t zero_bytes;  // the counter
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
@@ -39,10 +39,9 @@ __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t ma
   const size_t o_lg = 256;
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
-  w.items = reinterpret_cast<uint32_t*>(p);
+  w.items = reinterpret_cast<unsigned long long*>(p);
   w.logits = reinterpret_cast<float*>(p + o_lg);
   w.ldw = ldw;
-  w.zero_bytes = 16;
   if (total) *total = o_lg + ws_align((size_t)rows * ldw * 4);
   return w;
 }
@@ -57,7 +56,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   const int64_t r = blockIdx.x / parts;
   const int b = (int)(r / next_n), j = (int)(r % next_n);
   // an input of the call, read before the wait: this launch can only have
-  // started after the zero kernel's wait, i.e. after every kernel issued
+  // started after the scoring pass's wait, i.e. after every kernel issued
   // before the call completed
   int64_t L = __ldg(p.context_lens + b);
   pdl_wait();  // the scoring pass's logits
@@ -68,16 +67,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   // the workspace rows are 256-byte aligned
   cluster_select_row(sm, ws.logits + r * ws.ldw, len, (uint32_t)p.topk, p.out_idx + r * p.topk,
                      parts);
-}
-
-// Zeroes the scoring pass's work-item counter.  It waits for every earlier
-// kernel (the previous call's are done with the workspace) before it lets
-// the scoring pass start, so the kernels after it may read the call's inputs
-// before their own waits.
-__global__ void __launch_bounds__(32) paged_ws_zero_kernel(uint32_t* counter) {
-  pdl_wait();
-  if (threadIdx.x == 0) *counter = 0u;
-  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -103,19 +92,13 @@ cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cuda
   const int64_t rows = (int64_t)a.B * next_n;
   const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr);
   const size_t smem = sizeof(SelSmem);
-  // the three kernels share one shared-memory carveout, so no SM has to be
+  // the two kernels share one shared-memory carveout, so no SM has to be
   // reconfigured between them
-  cudaError_t e = cudaFuncSetAttribute(paged_ws_zero_kernel,
-                                       cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(paged_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(paged_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  e = launch_dependent(paged_ws_zero_kernel, dim3(1), dim3(32), 0, stream, ws.items);
   if (e != cudaSuccess) return e;
   // scoring pass: the logits kernel writing into the workspace, work items
   // handed out by the counter
@@ -124,6 +107,7 @@ cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cuda
   s.ld = ws.ldw;
   s.clean = 0;
   s.item_counter = ws.items;
+  s.wait_first = 1;
   e = launch_paged_logits(H, next_n, s, stream);
   if (e != cudaSuccess) return e;
   const int parts = select_parts(paged_select_kernel, 0, rows, ws.ldw, a.sms > 0 ? a.sms : 1, smem);

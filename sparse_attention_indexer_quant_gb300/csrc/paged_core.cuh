@@ -247,6 +247,43 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     pdl_launch_dependents();
     pdl_wait();
   }
+  // The item loader's operands (warp 5), read into registers before they are
+  // staged, all loads of a lane in flight together:
+  //   B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
+  //   stored with the 64-byte swizzle (16-byte chunk c of row r at chunk
+  //   c ^ ((r >> 1) & 3)); its scale factors in the 32x16-byte atom (row r's
+  //   4 bytes at 16*(r % 32) + 4*(r / 32), rows past NH zero); the weights;
+  //   the page ids of the item's first n_tiles tiles (entries past the
+  //   sequence's last page are never used: the producers skip those pages).
+  constexpr int kQv = NH * 4 / 32;
+  uint4 qv_r[kQv];
+  uint32_t sf_r[4];
+  float w_r[NH / 32];
+  int32_t id_r[4];
+  auto load_operands = [&](int32_t b, int64_t k0, int32_t n_tiles) {
+    const uint4* qv = reinterpret_cast<const uint4*>(p.q_vals + (int64_t)b * NH * kValBytes);
+#pragma unroll
+    for (int u = 0; u < kQv; ++u) qv_r[u] = __ldg(qv + lane + 32 * u);
+    const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)b * NH;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sf_r[u] = lane + 32 * u < NH ? __ldg(qs + lane + 32 * u) : 0u;
+#pragma unroll
+    for (int u = 0; u < NH / 32; ++u) w_r[u] = __ldg(p.weights + (int64_t)b * NH + lane + 32 * u);
+    const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks + k0 / kPage;
+    const int64_t in_row = (int64_t)p.max_blocks - k0 / kPage;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = lane + 32 * u;
+      id_r[u] = i < 2 * n_tiles && i < in_row ? __ldg(bt + i) : 0;
+    }
+  };
+  // The loader's first item is this CTA's own index: its operands are read
+  // now, for all of the item's tiles, while the block fills the context-length
+  // cache that decides how many of them are used.
+  const bool preloaded = warp == 5 && (int64_t)blockIdx.x < (int64_t)p.B * p.chunks;
+  if (preloaded)
+    load_operands((int32_t)(blockIdx.x % p.B),
+                  (int64_t)(blockIdx.x / p.B) * p.tiles_per_cta * kTileKeys, p.tiles_per_cta);
   for (int i = threadIdx.x; i < p.B && i < kClCache; i += kPagedThreads)
     sCl[i] = __ldg(p.context_lens + i);
   Ep::init(extra);
@@ -284,37 +321,8 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
         it = paged_item(p, w, sCl, lane == 0);
         if (it.n_tiles > 0 || pass_empty) break;
       }
-      // the item's operands are read into registers before waiting for its
-      // buffer, all loads of a lane in flight together:
-      //   B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
-      //   stored with the 64-byte swizzle (16-byte chunk c of row r at chunk
-      //   c ^ ((r >> 1) & 3)); its scale factors in the 32x16-byte atom (row
-      //   r's 4 bytes at 16*(r % 32) + 4*(r / 32), rows past NH zero); the
-      //   weights; the item's page ids.
-      constexpr int kQv = NH * 4 / 32;
-      uint4 qv_r[kQv];
-      uint32_t sf_r[4];
-      float w_r[NH / 32];
-      int32_t id_r[4];
-      if (it.n_tiles > 0) {
-        const uint4* qv = reinterpret_cast<const uint4*>(p.q_vals + (int64_t)it.b * NH * kValBytes);
-#pragma unroll
-        for (int u = 0; u < kQv; ++u) qv_r[u] = __ldg(qv + lane + 32 * u);
-        const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)it.b * NH;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sf_r[u] = lane + 32 * u < NH ? __ldg(qs + lane + 32 * u) : 0u;
-#pragma unroll
-        for (int u = 0; u < NH / 32; ++u) w_r[u] = __ldg(p.weights + (int64_t)it.b * NH + lane + 32 * u);
-        // page ids of the item's tiles (the entries past the sequence's last
-        // page are never used: the producers skip those pages)
-        const int32_t* bt = p.block_table + (int64_t)it.b * p.max_blocks + it.k0 / kPage;
-        const int64_t in_row = (int64_t)p.max_blocks - it.k0 / kPage;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = lane + 32 * u;
-          id_r[u] = i < 2 * it.n_tiles && i < in_row ? __ldg(bt + i) : 0;
-        }
-      }
+      if (it.n_tiles > 0 && !(preloaded && w == (int64_t)blockIdx.x))
+        load_operands(it.b, it.k0, it.n_tiles);
       const int qb = n & 1;
       if (!__all_sync(kAll, mbar_wait(qempty_bar(qb), ((n >> 1) & 1) ^ 1, abort))) {
         if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);

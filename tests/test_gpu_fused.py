@@ -147,3 +147,36 @@ def test_fused_more_sequences_than_the_length_cache(idx, oracle):
     g = run_fused(idx, p, 2048)
     for b, (ol, om, L) in oracle_rows(oracle, p, [0, 517, 1024, 1029]).items():
         check_topk(g[b], ol[0, :L], om[0, :L], L, 2048, f"seq {b}")
+
+
+def test_fused_workspace_garbage_and_reuse(idx, oracle):
+    """The workspace needs no initialisation and may be shared by calls of
+    different shapes: the work-item counter starts from whatever the scratch
+    holds (random bytes here, with a counter value close to carrying into its
+    generation bits) and from the previous call's value."""
+    probs = [wl.make_decode("a", 921, [4100, 9000, 300, 20000], 32, 1),
+             wl.make_decode("b", 922, [8193, 50, 16000], 32, 2)]
+    need = max(idx.paged_logits_topk_workspace_bytes(p.B, p.next_n, p.block_table.shape[1], 2048)
+               for p in probs)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+    ws[:8] = torch.tensor(np.array([(0xABCDE12345 << 24) | 0xFFFFF0], np.uint64).view(np.uint8),
+                          device="cuda")
+    state = []
+    for p in probs:
+        cache = dev(wl.poisoned_cache(p.num_blocks))
+        idx.quant_insert(dev_bf16(p.k), dev(p.slots), cache)
+        qv, qs = idx.quant_q(dev_bf16(p.q))
+        state.append((p, cache, qv, qs, oracle_rows(oracle, p, range(p.B))))
+    for p, cache, qv, qs, ref in state + state[:1]:
+        errs = idx.new_errors()
+        out = idx.paged_logits_topk(qv, qs, dev(p.weights), cache, dev(p.block_table),
+                                    dev(p.context_lens), p.next_n, p.H, 2048, workspace=ws,
+                                    errors=errs)
+        torch.cuda.synchronize()
+        assert errs.cpu().tolist() == [0, 0]
+        g = out.cpu().numpy()
+        for b, (ol, om, L) in ref.items():
+            for j in range(p.next_n):
+                n = max(L - p.next_n + j + 1, 0)
+                check_topk(g[b * p.next_n + j], ol[j, :n], om[j, :n], n, 2048,
+                           f"{p.name} seq {b} row {j}")

@@ -180,3 +180,17 @@ def test_fused_workspace_garbage_and_reuse(idx, oracle):
                 n = max(L - p.next_n + j + 1, 0)
                 check_topk(g[b * p.next_n + j], ol[j, :n], om[j, :n], n, 2048,
                            f"{p.name} seq {b} row {j}")
+
+
+def test_fused_more_sequences_than_ctas(idx, oracle):
+    """With more sequences than persistent CTAs some sequences get no CTA's
+    first work item and are reached only through the counter; zero-length and
+    long sequences mixed."""
+    rng = np.random.default_rng(931)
+    lens = [int(x) for x in rng.integers(0, 3000, size=500)]
+    for b, L in [(0, 0), (3, 20000), (455, 9000), (456, 12345), (457, 0), (499, 31000)]:
+        lens[b] = L
+    p = wl.make_decode("t", 931, lens, 32, 1)
+    g = run_fused(idx, p, 2048)
+    for b, (ol, om, L) in oracle_rows(oracle, p, [0, 1, 3, 200, 455, 456, 457, 498, 499]).items():
+        check_topk(g[b], ol[0, :L], om[0, :L], L, 2048, f"seq {b}")

@@ -45,6 +45,7 @@ static_assert(kSubBins == 8 * 32, "one warp resolves the sub-bin, eight bins a l
 
 struct SelSmem {
   uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
+  uint32_t tsum[kSelThreads];  // per thread: its eight bins' slice count (read by the cluster)
   uint32_t sub[kSubBins];      // the candidates by their next 8 key bits (leader)
   uint32_t hist[kRadixBins];   // radix-digit scratch (leader)
   ScanScratch s;
@@ -195,40 +196,59 @@ __device__ __forceinline__ void cluster_select_row(SelSmem& sm, const float* x, 
     hist_keys(sm.bins, ka, s0 + c * kSelChunk, s1, t);
     hist_keys(sm.bins, kb, s0 + (c + 1) * kSelChunk, s1, t);
   }
-  cluster_sync_all();  // #1: every CTA's slice histogram is complete, the counters zeroed
-  // thread t's bins 4088 - 8t + j (j = 0..7), summed over the cluster (all of
-  // a thread's remote loads are issued before any is used)
-  uint32_t h8[8], local = 0;
+  __syncthreads();  // the slice histogram is complete
+  // thread t owns bins 4088 - 8t + j (j = 0..7): its slice counts, and their
+  // sum, published for the cluster
+  uint32_t h8[8];
   {
+    const uint4 lo = *reinterpret_cast<const uint4*>(&sm.bins[kCoarseBins - 8 - 8 * t]);
+    const uint4 hi = *reinterpret_cast<const uint4*>(&sm.bins[kCoarseBins - 4 - 8 * t]);
+    h8[0] = lo.x;
+    h8[1] = lo.y;
+    h8[2] = lo.z;
+    h8[3] = lo.w;
+    h8[4] = hi.x;
+    h8[5] = hi.y;
+    h8[6] = hi.z;
+    h8[7] = hi.w;
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) local += h8[j];
+  sm.tsum[t] = local;
+  cluster_sync_all();  // #1: every CTA's slice sums are published, the counters zeroed
+  {  // the row's count over thread t's bins (the other slices' sums in flight together)
+    const uint32_t my = smem_u32(&sm.tsum[t]);
+    uint32_t r[kMaxParts];
+#pragma unroll
+    for (int q = 0; q < kMaxParts; ++q)
+      r[q] = q < parts && q != part ? ld_cluster_u32(cluster_map(my, (uint32_t)q)) : 0u;
+#pragma unroll
+    for (int q = 0; q < kMaxParts; ++q) local += r[q];
+  }
+  const uint32_t excl = block_exclusive_scan(local, sm.s);
+  if (excl < k && k <= excl + local) {  // the thread holding the k-th largest
+    // the row's counts of its eight bins: the other slices' through DSMEM
     const uint32_t my0 = smem_u32(&sm.bins[kCoarseBins - 8 - 8 * t]);
-    const uint32_t my1 = my0 + 16u;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     uint4 v[2 * kMaxParts];
 #pragma unroll
     for (int q = 0; q < kMaxParts; ++q) {
-      v[2 * q] = q < parts ? ld_cluster_v4(cluster_map(my0, q)) : z;
-      v[2 * q + 1] = q < parts ? ld_cluster_v4(cluster_map(my1, q)) : z;
+      const bool other = q < parts && q != part;
+      v[2 * q] = other ? ld_cluster_v4(cluster_map(my0, (uint32_t)q)) : z;
+      v[2 * q + 1] = other ? ld_cluster_v4(cluster_map(my0 + 16u, (uint32_t)q)) : z;
     }
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 a = v[half];
-#pragma unroll
-      for (int q = 1; q < kMaxParts; ++q) {
-        a.x += v[2 * q + half].x;
-        a.y += v[2 * q + half].y;
-        a.z += v[2 * q + half].z;
-        a.w += v[2 * q + half].w;
-      }
-      h8[4 * half + 0] = a.x;
-      h8[4 * half + 1] = a.y;
-      h8[4 * half + 2] = a.z;
-      h8[4 * half + 3] = a.w;
+    for (int q = 0; q < kMaxParts; ++q) {
+      h8[0] += v[2 * q].x;
+      h8[1] += v[2 * q].y;
+      h8[2] += v[2 * q].z;
+      h8[3] += v[2 * q].w;
+      h8[4] += v[2 * q + 1].x;
+      h8[5] += v[2 * q + 1].y;
+      h8[6] += v[2 * q + 1].z;
+      h8[7] += v[2 * q + 1].w;
     }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) local += h8[j];
-  const uint32_t excl = block_exclusive_scan(local, sm.s);
-  if (excl < k && k <= excl + local) {
     uint32_t run = excl;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {  // bins 4095 - 8t - q, highest first

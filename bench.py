@@ -335,7 +335,8 @@ def run_ours(args, rank, world, local_rank):
 
     also = None
     if rank == 0 and not args.no_also:
-        also = secondary_measurements(idx, dev, flush_l2, stream)
+        also = secondary_measurements(idx, dev, flush_l2, stream,
+                                      decode=(p, cache, qv, qs, w, bt, cl))
 
     cpu = None
     if rank == 0:
@@ -402,12 +403,35 @@ def time_op(fn, flush_l2, stream, reps):
     return ts[len(ts) // 2]
 
 
-def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
-    """Insert throughput and prefill logits / top-k on the 32K-token causal
-    prefill (one sequence, H = 32), each timed alone with a flushed L2."""
+def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
+    """The other steps of the path, each timed alone with a flushed L2: insert,
+    q-quant, gather, prefill logits and top-k on the 32K-token causal prefill
+    (one sequence, H = 32); with `decode` (the batched decode state), the
+    unfused paged logits and the top-k of its rows."""
     import torch
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     hbm, _ = peaks()
+    res = {}
+    if decode is not None:
+        dp, dcache, dqv, dqs, dw, dbt, dcl = decode
+        ld = dp.block_table.shape[1] * 64
+        lg = torch.empty((dp.rows, ld), dtype=torch.float32, device=dev)
+        pl_ms = time_op(lambda: idx.paged_mqa_logits(dqv, dqs, dw, dcache, dbt, dcl, dp.next_n,
+                                                     dp.H, ld=ld, out=lg), flush_l2, stream, reps)
+        st_r, en_r = dp.row_windows()
+        n_logits = int((en_r.astype(np.int64) - st_r).sum())
+        pl_bytes = fused_algorithmic_bytes(dp) - dp.rows * dp.topk * 4 + 4 * n_logits
+        en_d = torch.from_numpy(en_r).to(dev)
+        dout = torch.empty((dp.rows, TOPK), dtype=torch.int32, device=dev)
+        dk_ms = time_op(lambda: idx.topk_rows(lg, en_d, TOPK, out=dout), flush_l2, stream, reps)
+        res["paged_logits_unfused"] = {
+            "workload": "batched decode, logits rows written to HBM (unclean)", "ms": pl_ms,
+            "gbs": pl_bytes / (pl_ms * 1e-3) / 1e9,
+            "frac_of_hbm": pl_bytes / (pl_ms * 1e-3) / 1e9 / hbm}
+        res["decode_topk_rows"] = {
+            "workload": "the batched decode's 64 logits rows, k=2048", "ms": dk_ms,
+            "read_gbs": (4 * n_logits + dp.rows * TOPK * 4) / (dk_ms * 1e-3) / 1e9}
+        del lg
     p = wl.prefill()
     S = int(p.tok_offsets[-1])
     cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
@@ -418,7 +442,14 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
     kv, ks = idx.gather_k(cache, torch.from_numpy(p.block_table).to(dev),
                           torch.from_numpy(p.new_lens.astype(np.int32)).to(dev),
                           torch.zeros(1, dtype=torch.int64, device=dev), S)
-    qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+    g_bt = torch.from_numpy(p.block_table).to(dev)
+    g_lens = torch.from_numpy(p.new_lens.astype(np.int32)).to(dev)
+    g_off = torch.zeros(1, dtype=torch.int64, device=dev)
+    g_ms = time_op(lambda: idx.gather_k(cache, g_bt, g_lens, g_off, S), flush_l2, stream, reps)
+    q_bf = bf16_tensor(p.q, dev)
+    qv, qs = idx.quant_q(q_bf)
+    qq_ms = time_op(lambda: idx.quant_q(q_bf, out_vals=qv, out_scales=qs), flush_l2, stream, reps)
+    q_rows = p.T * p.H
     w = torch.from_numpy(p.weights).to(dev)
     st, en = p.windows()
     st_d, en_d = torch.from_numpy(st).to(dev), torch.from_numpy(en).to(dev)
@@ -433,7 +464,13 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
                       flush_l2, stream, reps)
     del logits
     tf = flops / (pre_ms * 1e-3) / 1e12
-    return {
+    res.update({
+        "q_quant": {"workload": f"{q_rows} query-head rows of the causal prefill", "ms": qq_ms,
+                    "gbs": q_rows * (256 + 68) / (qq_ms * 1e-3) / 1e9,
+                    "frac_of_hbm": q_rows * (256 + 68) / (qq_ms * 1e-3) / 1e9 / hbm},
+        "gather": {"workload": "32768 cached keys of the causal prefill", "ms": g_ms,
+                   "gbs": S * 2 * 68 / (g_ms * 1e-3) / 1e9,
+                   "frac_of_hbm": S * 2 * 68 / (g_ms * 1e-3) / 1e9 / hbm},
         "insert": {"workload": "32768 bf16 keys of the causal prefill", "ms": ins_ms,
                    "tokens_per_s": S / (ins_ms * 1e-3),
                    "gbs": ins_bytes / (ins_ms * 1e-3) / 1e9,
@@ -445,7 +482,8 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10):
                            "valid_pairs": pairs},
         "prefill_topk": {"workload": "32768 causal rows, k=2048", "ms": topk_ms,
                          "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9},
-    }
+    })
+    return res
 
 
 def cpu_baseline(p, n_seq, min_seconds=10.0, max_steps=200):

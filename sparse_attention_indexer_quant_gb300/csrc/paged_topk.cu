@@ -13,8 +13,9 @@
 // inputs before waiting for the logits.
 //
 // Workspace (device, caller-owned), 256-byte aligned pieces: the u64 work-item
-// counter (no clearing needed: see claim_item), then f32 logits [rows][ldw],
-// ldw = max_blocks * 64.
+// counter (tagged with the call's generation, see claim_item; the select
+// clears it at the end of every call, which keeps replays of a captured call
+// correct), then f32 logits [rows][ldw], ldw = max_blocks * 64.
 #include <math.h>
 
 #include "common.cuh"
@@ -60,6 +61,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   // before the call completed
   int64_t L = __ldg(p.context_lens + b);
   pdl_wait();  // the scoring pass's logits
+  // the work-item counter is done with: clear it, so that a replay of this
+  // call with the same generation (a CUDA graph) finds no claims of its own
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ws.items = 0ull;
   const int64_t cap = (int64_t)p.max_blocks * kPage;
   L = L < 0 ? 0 : (L > cap ? cap : L);
   int64_t len = L - next_n + j + 1;

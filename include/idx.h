@@ -33,6 +33,9 @@
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates no device memory and never synchronises; work is enqueued on
  *     `stream` (NULL = the legacy default stream) and the call returns at once.
+ *     So every call can be captured in a CUDA graph; a replay reads its
+ *     buffers afresh (the fused call's work-item counter starts over on every
+ *     replay).
  *   - Argument and device errors are returned synchronously, before anything is
  *     enqueued.  IDX_ERR_CUDA reports a launch failure (the CUDA error string
  *     is available from idx_last_error_detail()).

@@ -13,8 +13,8 @@
 //               writes them in the 32x16-byte scale-factor layout, tcgen05.cp to
 //               TMEM, and two tcgen05.mma kind::mxf4 (K = 64 each) into a
 //               128 x 256 fp32 accumulator;
-//   warps 2-9   epilogue: TMEM lane = key; each pair of warps on a lane quarter
-//               splits the G queries; w * max(0, .) summed over heads, masked
+//   warps 2-17  epilogue: TMEM lane = key; the four warps on a lane quarter
+//               split the G queries; w * max(0, .) summed over heads, masked
 //               to each query's window.
 // The CTA order is reversed so that the largest groups (the end of a causal
 // prefill) start first.
@@ -27,10 +27,10 @@
 namespace idx {
 namespace {
 
-constexpr int kMqaThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kMqaThreads = 576;   // warp 0 TMA, warp 1 MMA, warps 2-17 epilogue
 constexpr int kMqaStages = 4;
 constexpr int kN = 256;            // query-head columns per CTA
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 
 struct MqaLayout {
   static constexpr uint32_t kAccCol = 0;            // 256 fp32 columns
@@ -53,7 +53,7 @@ template <int H>
 __global__ void __launch_bounds__(kMqaThreads, 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_k, const MqaArgs p) {
   constexpr int G = kN / H;       // queries per CTA
-  constexpr int GH = G / 2;       // queries per epilogue warp
+  constexpr int GH = G / 4;       // queries per epilogue warp
   using Lay = MqaLayout;
   const int64_t n_groups = (p.T + G - 1) / G;
   const int64_t g = n_groups - 1 - (int64_t)blockIdx.x;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
     // ---------------------------------------------------------- epilogue
     const int e = warp - 2;
     const int quarter = warp & 3;
-    const int half = e / 4;                 // which half of the group's queries
+    const int half = e / 4;                 // which quarter of the group's queries
     const int m = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     int32_t st[GH], en[GH];

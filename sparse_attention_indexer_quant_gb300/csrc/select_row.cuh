@@ -36,12 +36,9 @@ constexpr int kSelChunk = kSelThreads * 4 * kSelVec;    // 8192 elements
 constexpr int kCandSmem = 8192;                         // boundary-bin elements in the leader
 constexpr int kMaxParts = 4;                            // CTAs per row at most
 constexpr int kMinSlice = 4096;                         // elements per CTA at least
-constexpr int kSubShift = 12;                           // sub-bin: key bits 19..12
-constexpr int kSubBins = 256;
 constexpr int kList2 = 2048;                            // boundary sub-bin list (leader)
 constexpr int kRankDirect = 64;                         // sub-bin lists ranked element by element
 static_assert(kCoarseBins == 8 * kSelThreads, "each select thread owns eight histogram bins");
-static_assert(kSubBins == 8 * 32, "one warp resolves the sub-bin, eight bins a lane");
 
 struct SelSmem {
   uint32_t bins[kCoarseBins];  // coarse histogram of this CTA's slice
@@ -116,37 +113,6 @@ __device__ __forceinline__ void hist_keys(uint32_t* bins, const uint4 (&kv)[kSel
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (i0 + q < s1) atomicAdd(&bins[coarse_bin(e4[q])], 1u);
-    }
-  }
-}
-
-// In warp 0 of the block: the bin b of hist[0, kSubBins) with
-// count(bins > b) < need <= count(bins >= b) -> sc.bin, and count(bins > b)
-// -> sc.above.  Requires 1 <= need <= the total count.
-__device__ __forceinline__ void warp_find_sub_bin(const uint32_t* hist, uint32_t need,
-                                                  ScanScratch& sc) {
-  const int lane = threadIdx.x & 31;
-  uint32_t h[8], local = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {  // bins kSubBins - 1 - 8 * lane - q, highest first
-    h[q] = hist[kSubBins - 1 - 8 * lane - q];
-    local += h[q];
-  }
-  uint32_t incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  uint32_t run = incl - local;
-  if (run < need && need <= incl) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (run < need && need <= run + h[q]) {
-        sc.bin = (uint32_t)(kSubBins - 1 - 8 * lane - q);
-        sc.above = run;
-      }
-      run += h[q];
     }
   }
 }

@@ -10,11 +10,11 @@
 //      the packed counts gives each thread its output and candidate offsets, so
 //      the elements above b1 go straight to out and b1's elements to a
 //      shared-memory candidate list without atomics;
-//   3. the exact remainder among b1's elements: when they are at most the
-//      thread count, each thread ranks one of them against all the others
-//      (value, then position) and the ones ranked below the remaining count
-//      take the slots after the elements above b1; otherwise two 10-bit radix
-//      digits on the key bits below the bin.
+//   3. the exact remainder among b1's elements: their next 8 key bits give
+//      the sub-bin holding the k-th largest (one warp scans the 256 counts);
+//      the elements above it take the next slots, and the few in it are
+//      ranked against each other (value, then position), or resolved by radix
+//      digits on the low 12 key bits when there are many.
 // A row of at most CHUNK elements is read from global memory once.  If b1
 // holds more elements than the candidate list, step 3 runs its radix passes
 // over the row itself, restricted to b1.
@@ -27,6 +27,8 @@ namespace idx {
 
 constexpr int kRowThreads = 512;
 constexpr int kRowCandCap = 4096;
+constexpr int kRowList2 = 2048;      // sub-bin list, in the spent staging buffer
+constexpr int kRowRankDirect = 64;   // sub-bin lists ranked element by element
 
 template <int CHUNK>
 struct RowTopkSmem {
@@ -36,7 +38,9 @@ struct RowTopkSmem {
   uint32_t out_base;
   uint32_t cand_base;
   uint32_t slot;
+  uint32_t n2;
   uint32_t keys[CHUNK];
+  static_assert(CHUNK >= 2 * kRowList2, "the sub-bin list lives in the staging buffer");
 };
 
 // The k largest of x[0, len) -> out[0, k) as positions 0..len-1 (any order),
@@ -133,30 +137,68 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
     __syncthreads();
   }
 
-  // ---- 3. the exact remainder inside b1
+  // ---- 3. the exact remainder inside b1: b1's elements by their next 8 key
+  //         bits (the sub-bin sb1 holding the k-th largest), those above sb1
+  //         to the output, then among sb1's few elements by rank (key, then
+  //         position), or by radix digits on the low 12 bits when there are
+  //         many
   const uint32_t need = (uint32_t)k - above;
-  if (nb1 <= (uint32_t)kRowThreads) {
-    if (threadIdx.x < nb1) {
-      const uint32_t key = sm.cand_keys[threadIdx.x];
-      const int32_t pos = sm.cand_idx[threadIdx.x];
+  if (threadIdx.x == 0) sm.slot = above;
+  auto emit = [&](uint32_t, int32_t i) { out[warp_claim(&sm.slot, true)] = i; };
+  if (!fits) {
+    __syncthreads();
+    const GlobalLogits<true> row{x, 0, len};
+    radix_select(sm.sel.hist, sm.sel.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+    return;
+  }
+  uint32_t* const sub = sm.sel.hist;  // the coarse histogram is spent
+  if (threadIdx.x < kSubBins) sub[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) sm.n2 = 0u;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < nb1; i += kRowThreads)
+    atomicAdd(&sub[(sm.cand_keys[i] >> kSubShift) & (kSubBins - 1)], 1u);
+  __syncthreads();
+  if (threadIdx.x < 32) warp_find_sub_bin(sub, need, sm.sel.s);
+  __syncthreads();
+  const uint32_t sb1 = sm.sel.s.bin;
+  const uint32_t above2 = sm.sel.s.above;  // b1's elements above sb1
+  uint32_t* const keys2 = sm.keys;          // sb1's elements (the staging buffer is spent)
+  int32_t* const idx2 = reinterpret_cast<int32_t*>(sm.keys + kRowList2);
+  for (uint32_t i = threadIdx.x; i < nb1; i += kRowThreads) {
+    const uint32_t key = sm.cand_keys[i];
+    const int32_t pos = sm.cand_idx[i];
+    const uint32_t sb = (key >> kSubShift) & (kSubBins - 1);
+    const uint32_t s = warp_claim(&sm.slot, sb > sb1);
+    if (sb > sb1) out[s] = pos;
+    const uint32_t s2 = warp_claim(&sm.n2, sb == sb1);
+    if (sb == sb1 && s2 < (uint32_t)kRowList2) {
+      keys2[s2] = key;
+      idx2[s2] = pos;
+    }
+  }
+  __syncthreads();
+  const uint32_t n2 = sm.n2;
+  const uint32_t need2 = need - above2;
+  if (n2 <= (uint32_t)kRowRankDirect) {
+    if (threadIdx.x < n2) {
+      const uint32_t key = keys2[threadIdx.x];
+      const int32_t pos = idx2[threadIdx.x];
       uint32_t rank = 0;
-      for (uint32_t q = 0; q < nb1; ++q) {
-        const uint32_t kq = sm.cand_keys[q];
-        rank += (kq > key || (kq == key && sm.cand_idx[q] < pos)) ? 1u : 0u;
+      for (uint32_t q = 0; q < n2; ++q) {
+        const uint32_t kq = keys2[q];
+        rank += (kq > key || (kq == key && idx2[q] < pos)) ? 1u : 0u;
       }
-      if (rank < need) out[above + rank] = pos;
+      if (rank < need2) out[above + above2 + rank] = pos;
     }
     return;
   }
-  if (threadIdx.x == 0) sm.slot = above;
-  __syncthreads();
-  auto emit = [&](uint32_t, int32_t i) { out[warp_claim(&sm.slot, true)] = i; };
-  if (fits) {
-    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
-    radix_select(sm.sel.hist, sm.sel.s, cand, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+  const uint32_t prefix = (b1 << kCoarseShift) | (sb1 << kSubShift);
+  if (n2 <= (uint32_t)kRowList2) {
+    const SmemPairs cand{keys2, idx2, (int)n2};
+    radix_select(sm.sel.hist, sm.sel.s, cand, need2, prefix, 32 - kSubShift, emit);
   } else {
-    const GlobalLogits<true> row{x, 0, len};
-    radix_select(sm.sel.hist, sm.sel.s, row, need, b1 << kCoarseShift, 32 - kCoarseShift, emit);
+    const SmemPairs cand{sm.cand_keys, sm.cand_idx, (int)nb1};
+    radix_select(sm.sel.hist, sm.sel.s, cand, need2, prefix, 32 - kSubShift, emit);
   }
 }
 

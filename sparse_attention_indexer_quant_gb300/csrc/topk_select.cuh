@@ -168,6 +168,42 @@ __device__ __forceinline__ void radix_select(uint32_t* hist, ScanScratch& sc, co
   __syncthreads();
 }
 
+// Sub-bin of a boundary bin: the next 8 key bits below the coarse 12.
+constexpr int kSubShift = 12;
+constexpr int kSubBins = 256;
+static_assert(kSubBins == 8 * 32, "one warp resolves the sub-bin, eight bins a lane");
+
+// In warp 0 of the block: the bin b of hist[0, kSubBins) with
+// count(bins > b) < need <= count(bins >= b) -> sc.bin, and count(bins > b)
+// -> sc.above.  Requires 1 <= need <= the total count.
+__device__ __forceinline__ void warp_find_sub_bin(const uint32_t* hist, uint32_t need,
+                                                  ScanScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h[8], local = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {  // bins kSubBins - 1 - 8 * lane - q, highest first
+    h[q] = hist[kSubBins - 1 - 8 * lane - q];
+    local += h[q];
+  }
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t run = incl - local;
+  if (run < need && need <= incl) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run < need && need <= run + h[q]) {
+        sc.bin = (uint32_t)(kSubBins - 1 - 8 * lane - q);
+        sc.above = run;
+      }
+      run += h[q];
+    }
+  }
+}
+
 // Elements of a shared-memory array of keys with their indices.
 struct SmemPairs {
   const uint32_t* keys;

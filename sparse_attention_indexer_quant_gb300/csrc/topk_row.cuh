@@ -2,22 +2,25 @@
 // "vllm.models.glm5next.nvidia.sparse_indexer": top_k_per_row into
 // topk_indices_buffer; rows shorter than k are padded with -1).
 //
-// The row is processed in chunks of CHUNK elements staged in shared memory:
+// A row whose start is 16-byte aligned is streamed from global memory (L2 on
+// the second pass) in rounds of float4 loads, eight of a thread's in flight;
+// other rows are staged in shared memory in chunks of CHUNK elements:
 //   1. coarse histogram of the row (top 12 key bits: sign, exponent and three
-//      mantissa bits) while the chunk is loaded; the bin b1 holding the k-th
-//      largest value and the count above it follow from one block-wide scan;
-//   2. every thread counts its elements above b1 and in b1; one block scan of
-//      the packed counts gives each thread its output and candidate offsets, so
-//      the elements above b1 go straight to out and b1's elements to a
-//      shared-memory candidate list without atomics;
+//      mantissa bits); the bin b1 holding the k-th largest value and the count
+//      above it follow from one block-wide scan;
+//   2. streamed rows: each thread classifies its elements of a round as above
+//      b1 or in it (bit masks) and a warp takes its output and candidate slots
+//      with one shared-memory atomic add per list; staged rows: per chunk, one
+//      block scan of the packed counts gives each thread its offsets.  The
+//      elements above b1 go straight to out, b1's elements to a shared-memory
+//      candidate list;
 //   3. the exact remainder among b1's elements: their next 8 key bits give
 //      the sub-bin holding the k-th largest (one warp scans the 256 counts);
 //      the elements above it take the next slots, and the few in it are
 //      ranked against each other (value, then position), or resolved by radix
 //      digits on the low 12 key bits when there are many.
-// A row of at most CHUNK elements is read from global memory once.  If b1
-// holds more elements than the candidate list, step 3 runs its radix passes
-// over the row itself, restricted to b1.
+// If b1 holds more elements than the candidate list, step 3 runs its radix
+// passes over the row itself, restricted to b1.
 #pragma once
 
 #include "common.cuh"
@@ -27,6 +30,7 @@ namespace idx {
 
 constexpr int kRowThreads = 512;
 constexpr int kRowCandCap = 4096;
+constexpr int kRowVec = 8;           // float4 loads of a thread in flight per round
 constexpr int kRowList2 = 2048;      // sub-bin list, in the spent staging buffer
 constexpr int kRowRankDirect = 64;   // sub-bin lists ranked element by element
 
@@ -42,6 +46,19 @@ struct RowTopkSmem {
   uint32_t keys[CHUNK];
   static_assert(CHUNK >= 2 * kRowList2, "the sub-bin list lives in the staging buffer");
 };
+
+// Element `bit` (float4 bit >> 2, lane bit & 3) of a thread's round, picked by
+// selects rather than an indexed (local-memory) array access.
+__device__ __forceinline__ float round_value(const float4 (&v)[kRowVec], int bit) {
+  static_assert(kRowVec == 8, "three select levels");
+  const int u = bit >> 2;
+  const float4 a01 = (u & 1) ? v[1] : v[0], a23 = (u & 1) ? v[3] : v[2];
+  const float4 a45 = (u & 1) ? v[5] : v[4], a67 = (u & 1) ? v[7] : v[6];
+  const float4 b0 = (u & 2) ? a23 : a01, b1 = (u & 2) ? a67 : a45;
+  const float4 c = (u & 4) ? b1 : b0;
+  const float lo = (bit & 1) ? c.y : c.x, hi = (bit & 1) ? c.w : c.z;
+  return (bit & 2) ? hi : lo;
+}
 
 // The k largest of x[0, len) -> out[0, k) as positions 0..len-1 (any order),
 // -1 padded.  All threads of the CTA call it.
@@ -84,9 +101,49 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
     return n;
   };
 
-  // ---- 1. coarse histogram
+  // ---- 1. coarse histogram.  A 16-byte aligned row is streamed with float4
+  //         loads, eight of a thread's in flight at once (16384 elements of
+  //         the row per round); other rows are staged chunk by chunk.
   int n_last = 0;
-  for (int c = 0; c < n_chunks; ++c) n_last = stage(c, true);
+  const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  // a round: thread t's float4 u covers elements base + 4 * (u * 512 + t) ..+3
+  auto load_round = [&](int64_t base, float4 (&v)[kRowVec]) {
+#pragma unroll
+    for (int u = 0; u < kRowVec; ++u) {
+      const int64_t i0 = base + 4 * ((int64_t)u * kRowThreads + threadIdx.x);
+      if (i0 + 3 < len) {
+        v[u] = __ldcg(reinterpret_cast<const float4*>(x + i0));
+      } else {
+        v[u].x = i0 + 0 < len ? __ldcg(x + i0 + 0) : 0.f;
+        v[u].y = i0 + 1 < len ? __ldcg(x + i0 + 1) : 0.f;
+        v[u].z = i0 + 2 < len ? __ldcg(x + i0 + 2) : 0.f;
+        v[u].w = i0 + 3 < len ? __ldcg(x + i0 + 3) : 0.f;
+      }
+    }
+  };
+  constexpr int64_t kRound = (int64_t)kRowVec * 4 * kRowThreads;
+  if (aligned) {
+    constexpr int kVec = kRowVec;
+    for (int64_t base = 0; base < len; base += kRound) {
+      float4 v[kVec];
+      load_round(base, v);
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) {
+        const int64_t i0 = base + 4 * ((int64_t)u * kRowThreads + threadIdx.x);
+        const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (i0 + q < len) {
+            const uint32_t key = float_key(e4[q]);
+            atomicAdd(&sm.sel.hist[coarse_bin(key)], 1u);
+          }
+        }
+      }
+    }
+    n_last = (int)(len - (int64_t)(n_chunks - 1) * CHUNK);
+  } else {
+    for (int c = 0; c < n_chunks; ++c) n_last = stage(c, true);
+  }
   __syncthreads();
   find_threshold_bin(sm.sel.hist, kCoarseBins, (uint32_t)k, sm.sel.s);
   const uint32_t b1 = sm.sel.s.bin;
@@ -94,7 +151,64 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
   const uint32_t nb1 = sm.sel.hist[b1];
   const bool fits = nb1 <= (uint32_t)kRowCandCap;
 
-  // ---- 2. elements above b1 to out, b1's elements to the candidate list
+  // ---- 2. elements above b1 to out, b1's elements to the candidate list.
+  //         An aligned row is streamed again (it is in L2): each thread
+  //         classifies its elements of a round into bit masks, and a warp
+  //         takes its slots with one shared-memory atomic add per list.
+  if (aligned) {
+    const uint32_t key_b1 = b1 << kCoarseShift;
+    const uint32_t key_gt = key_b1 | ((1u << kCoarseShift) - 1u);
+    const int lane = threadIdx.x & 31;
+    for (int64_t base = 0; base < len; base += kRound) {
+      float4 v[kRowVec];
+      load_round(base, v);
+      uint32_t gt = 0u, eq = 0u;
+#pragma unroll
+      for (int u = 0; u < kRowVec; ++u) {
+        const int64_t i0 = base + 4 * ((int64_t)u * kRowThreads + threadIdx.x);
+        const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = float_key(e4[q]);
+          const bool in = i0 + q < len;
+          const uint32_t bit = 1u << (4 * u + q);
+          gt |= (key > key_gt && in) ? bit : 0u;
+          eq |= ((key ^ key_b1) < (1u << kCoarseShift) && in) ? bit : 0u;
+        }
+      }
+      const uint32_t ng = __popc(gt), ne = __popc(eq);
+      uint32_t ig = ng, ie = ne;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
+        const uint32_t ye = __shfl_up_sync(0xFFFFFFFFu, ie, o);
+        if (lane >= o) {
+          ig += yg;
+          ie += ye;
+        }
+      }
+      uint32_t bg = 0, be = 0;
+      if (lane == 31) {
+        if (ig != 0u) bg = atomicAdd(&sm.out_base, ig);
+        if (ie != 0u) be = atomicAdd(&sm.cand_base, ie);
+      }
+      uint32_t o = __shfl_sync(0xFFFFFFFFu, bg, 31) + ig - ng;
+      uint32_t cc = __shfl_sync(0xFFFFFFFFu, be, 31) + ie - ne;
+      auto pos = [&](int bit) -> int64_t {
+        return base + 4 * ((int64_t)(bit >> 2) * kRowThreads + threadIdx.x) + (bit & 3);
+      };
+      for (; gt != 0u; gt &= gt - 1u) out[o++] = (int32_t)pos(__ffs(gt) - 1);
+      for (; eq != 0u; eq &= eq - 1u) {
+        const int bit = __ffs(eq) - 1;
+        if (fits) {
+          sm.cand_keys[cc] = float_key(round_value(v, bit));
+          sm.cand_idx[cc] = (int32_t)pos(bit);
+        }
+        ++cc;
+      }
+    }
+    __syncthreads();
+  } else
   for (int c = 0; c < n_chunks; ++c) {
     int n = n_last;
     if (n_chunks > 1) {

@@ -29,10 +29,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
                      out + row * k, parts);
 }
 
-constexpr int kRowsChunk = 8192;
+constexpr int kRowsChunk = 4096;
 using RowsSmem = RowTopkSmem<kRowsChunk>;
 
-__global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(kRowThreads, 4) topk_rows_kernel(const float* __restrict__ logits,
                                                                 int64_t ld,
                                                                 const int32_t* row_start,
                                                                 const int32_t* row_end,

@@ -28,8 +28,8 @@
 
 namespace idx {
 
-constexpr int kRowThreads = 512;
-constexpr int kRowCandCap = 4096;
+constexpr int kRowThreads = 256;     // four CTAs (rows) per SM
+constexpr int kRowCandCap = 2048;
 constexpr int kRowVec = 8;           // float4 loads of a thread in flight per round
 constexpr int kRowList2 = 2048;      // sub-bin list, in the spent staging buffer
 constexpr int kRowRankDirect = 64;   // sub-bin lists ranked element by element
@@ -102,11 +102,11 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
   };
 
   // ---- 1. coarse histogram.  A 16-byte aligned row is streamed with float4
-  //         loads, eight of a thread's in flight at once (16384 elements of
+  //         loads, eight of a thread's in flight at once (8192 elements of
   //         the row per round); other rows are staged chunk by chunk.
   int n_last = 0;
   const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
-  // a round: thread t's float4 u covers elements base + 4 * (u * 512 + t) ..+3
+  // a round: thread t's float4 u covers elements base + 4 * (u * kRowThreads + t) ..+3
   auto load_round = [&](int64_t base, float4 (&v)[kRowVec]) {
 #pragma unroll
     for (int u = 0; u < kRowVec; ++u) {
@@ -216,7 +216,7 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
       n = stage(c, false);
       __syncthreads();
     }
-    // thread t takes elements t, t + 512, ... (conflict-free shared reads);
+    // thread t takes elements t, t + kRowThreads, ... (conflict-free shared reads);
     // its outputs go to a range of its own
     uint32_t n_gt = 0, n_eq = 0;
     for (int i = threadIdx.x; i < n; i += kRowThreads) {

@@ -266,7 +266,7 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
     return;
   }
   uint32_t* const sub = sm.sel.hist;  // the coarse histogram is spent
-  if (threadIdx.x < kSubBins) sub[threadIdx.x] = 0u;
+  for (int i = threadIdx.x; i < kSubBins; i += kRowThreads) sub[i] = 0u;
   if (threadIdx.x == 0) sm.n2 = 0u;
   __syncthreads();
   for (uint32_t i = threadIdx.x; i < nb1; i += kRowThreads)

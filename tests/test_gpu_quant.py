@@ -95,7 +95,7 @@ def test_insert_empty_is_noop(idx):
     assert torch.equal(cache, before)
 
 
-@pytest.mark.parametrize("rows", [1, 3 * 32, 64 * 2 * 64 + 5])
+@pytest.mark.parametrize("rows", [1, 3 * 32, 64 * 2 * 64 + 5, 65536, 65536 * 2 + 77])
 def test_quant_q_bit_exact(idx, oracle, rows):
     g = wl.rng(204 + rows)
     q = wl.normal_bf16(g, (rows, 128), wl.outlier_channels(g))

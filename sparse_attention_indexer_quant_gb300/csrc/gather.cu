@@ -19,7 +19,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_k_kernel(
     uint8_t* __restrict__ k_scales, int64_t out_rows, idx_device_errors* errors) {
   const int b = blockIdx.y;
   const int page_idx = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();  // inputs may come from the previous kernel
+  // the length, the page id and the output offset are read together (the
+  // page id of a page past the sequence is read but not used)
   int64_t len = __ldg(seq_lens + b);
+  const int32_t id = __ldg(bt + (int64_t)b * max_blocks + page_idx);
+  const int64_t base = __ldg(out_offsets + b);
   const int64_t cap = (int64_t)max_blocks * kPage;
   if (len < 0 || len > cap) {
     if (page_idx == 0 && threadIdx.x == 0) count_bad_input(errors);
@@ -27,7 +33,6 @@ __global__ void __launch_bounds__(kGatherThreads) gather_k_kernel(
   }
   const int64_t s0 = (int64_t)page_idx * kPage;
   if (s0 >= len) return;
-  const int32_t id = __ldg(bt + (int64_t)b * max_blocks + page_idx);
   if (id < 0 || id >= num_blocks) {
     if (threadIdx.x == 0) count_bad_input(errors);
     return;
@@ -35,7 +40,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_k_kernel(
   const int tok = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int64_t s = s0 + tok;
   if (s >= len) return;
-  const int64_t dst = __ldg(out_offsets + b) + s;
+  const int64_t dst = base + s;
   if (dst < 0 || dst >= out_rows) {
     if (part == 0) count_bad_input(errors);
     return;
@@ -56,11 +61,9 @@ cudaError_t launch_gather_k(const uint8_t* cache, int64_t num_blocks, const int3
                             uint8_t* k_scales, int64_t out_rows, idx_device_errors* errors,
                             cudaStream_t stream) {
   if (B == 0 || max_blocks == 0) return cudaSuccess;
-  dim3 grid((unsigned)max_blocks, (unsigned)B);
-  gather_k_kernel<<<grid, kGatherThreads, 0, stream>>>(cache, num_blocks, block_table, max_blocks,
-                                                       seq_lens, out_offsets, k_vals, k_scales,
-                                                       out_rows, errors);
-  return cudaGetLastError();
+  return launch_dependent(gather_k_kernel, dim3((unsigned)max_blocks, (unsigned)B),
+                          dim3(kGatherThreads), 0, stream, cache, num_blocks, block_table,
+                          max_blocks, seq_lens, out_offsets, k_vals, k_scales, out_rows, errors);
 }
 
 }  // namespace idx

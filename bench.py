@@ -559,25 +559,20 @@ def run_reference(args, rank, world):
     import oracle
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     p = make_workload(args.workload)
-    # calibrate the per-step sample so that warmup + steps take about 90 s
+    # calibrate the per-step sample so that warmup + steps take about 90 s: as
+    # many sequences as the oracle has threads (it parallelises over query
+    # rows), each window cut short to fit (the rate is per key-token)
     budget_s = args.ref_budget_s
     n_steps = args.steps + args.warmup
-    probe = cpu_baseline(p, 1, min_seconds=0.0)
+    n_seq = max(1, min(p.B, oracle.num_threads()))
+    probe = cpu_baseline(p, n_seq, min_seconds=0.0)
     rate = probe["value"]
-    per_step_tokens = max(2048, int(rate * budget_s / max(n_steps, 1)))
-    # sample: the first sequences whose windows fit per_step_tokens; a window may
-    # be cut short to fit (the rate is per key-token)
-    lens = p.context_lens.astype(np.int64)
-    n_seq = int(np.searchsorted(np.cumsum(lens), per_step_tokens, side="right"))
-    n_seq = max(1, min(n_seq, p.B))
-    cut = min(int(lens[:n_seq].sum()), per_step_tokens)
+    per_step_tokens = max(2048 * n_seq, int(rate * budget_s / max(n_steps, 1)))
+    per_seq = max(1, per_step_tokens // n_seq)
     cache = wl.poisoned_cache(p.num_blocks)
     hi_tok = int(p.tok_offsets[n_seq])
     oracle.quant_insert(p.k[:hi_tok], p.slots[:hi_tok], cache)
-    ctx = p.context_lens[:n_seq].copy()
-    over = int(ctx.astype(np.int64).sum()) - cut
-    if over > 0:
-        ctx[-1] = max(1, int(ctx[-1]) - over)
+    ctx = np.minimum(p.context_lens[:n_seq], per_seq).astype(np.int32)
     rows = n_seq * p.next_n
     new_rows = [r for r in p.new_token_rows() if r < hi_tok]
     ld = p.block_table.shape[1] * 64
@@ -598,8 +593,8 @@ def run_reference(args, rank, world):
     dt = time.perf_counter() - t0
     toks = int(ctx.astype(np.int64).sum())
     value = toks * args.steps / dt
-    sample = (f"first {n_seq} of {p.B} sequences, {toks} key-tokens per step "
-              f"(oracle decode step: insert, q-quant, logits, top-k)")
+    sample = (f"first {n_seq} of {p.B} sequences, contexts cut to at most {per_seq} keys, "
+              f"{toks} key-tokens per step (oracle decode step: insert, q-quant, logits, top-k)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,

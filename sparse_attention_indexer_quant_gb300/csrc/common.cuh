@@ -54,17 +54,6 @@ __device__ __forceinline__ float inv_scale_of(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
 }
 
-// E2M1 code of the bf16 value x scaled by inv_scale.  The product is exact for
-// every magnitude that can round to a nonzero code; the rounding is nearest
-// with ties to the even code, via threshold counts; the sign comes from x.
-__device__ __forceinline__ uint32_t e2m1_code(uint32_t x_bf16, float inv_scale) {
-  float a = fabsf(__uint_as_float((x_bf16 & 0x7FFFu) << 16) * inv_scale);
-  uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-               (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-               (uint32_t)(a > 5.0f);
-  return c | ((x_bf16 >> 12) & 0x8u);
-}
-
 // ---------------------------------------------------------------- smem / sync
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -242,15 +231,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int32_t x,
-                                            int32_t y, int32_t z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -336,10 +316,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // tmem_ld32 followed by the wait in the same statement, so that no use of the
 // loaded registers can be scheduled before the data has arrived.
 __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float (&v)[32]) {
@@ -366,14 +342,4 @@ __device__ __forceinline__ uint32_t float_key(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 }  // namespace idx

@@ -92,9 +92,6 @@ __device__ __forceinline__ int64_t len_cap(const PagedArgs& p) {
   if (p.logits != nullptr && p.ld < cap) cap = p.ld;
   return cap;
 }
-__device__ __forceinline__ int64_t clamp_len(int64_t L, int64_t cap) {
-  return L < 0 ? 0 : (L > cap ? cap : L);
-}
 
 // Work item w in chunk-major order: w = c * B + b.
 __device__ __forceinline__ ItemDesc paged_item(const PagedArgs& p, int64_t w, const int32_t* cl,

@@ -271,25 +271,4 @@ struct GlobalLogits {
   }
 };
 
-// dst[0, n) = src[0, n) (n a multiple of 4, both 16-byte aligned), all loads
-// of a thread issued before its stores.
-__device__ __forceinline__ void copy_words_cg(uint32_t* dst, const uint32_t* src, int n) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-  const int n4 = n / 4;
-  for (int base = 0; base < n4; base += 4 * blockDim.x) {
-    uint4 t[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = base + u * blockDim.x + threadIdx.x;
-      if (i < n4) t[u] = __ldcg(s4 + i);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = base + u * blockDim.x + threadIdx.x;
-      if (i < n4) d4[i] = t[u];
-    }
-  }
-}
-
 }  // namespace idx

@@ -107,3 +107,44 @@ def test_topk_rows_mostly_neg_inf(idx, n, finite):
         assert len(set(out[r].tolist())) == k
         if finite <= k:
             assert set(np.nonzero(np.isfinite(vals))[0].tolist()) <= set(out[r].tolist())
+
+
+def test_topk_many_rows_long_tied_and_unaligned(idx):
+    """More rows than SMs take the one-CTA-per-row kernel: long rows streamed
+    in several rounds (aligned starts), long rows staged in several chunks
+    (unaligned starts), rows whose boundary bin overflows the candidate list
+    (few distinct values, all equal), rows whose k-th value is -inf."""
+    g = wl.rng(440)
+    k = 2048
+    special = [(0, 20000, "rand"), (1, 70000, "rand"), (0, 30000, "ties"), (0, 10000, "equal"),
+               (2, 20000, "neginf"), (0, 20000, "neginf"), (3, 4097, "rand"), (0, 8193, "rand"),
+               (5, 2049, "rand"), (0, 0, "rand"), (0, 1, "rand"), (1, 9000, "ties3")]
+    n_rows = 200
+    starts = np.zeros(n_rows, np.int64)
+    lens = g.integers(100, 3000, size=n_rows)
+    for r, (s, n, _) in enumerate(special):
+        starts[r], lens[r] = s, n
+    ld = int((starts + lens).max()) + 12
+    ld += (-ld) % 4
+    logits = np.full((n_rows, ld), np.nan, np.float32)
+    for r in range(n_rows):
+        s, n = int(starts[r]), int(lens[r])
+        kind = special[r][2] if r < len(special) else "rand"
+        if kind == "rand":
+            row = g.standard_normal(n).astype(np.float32)
+        elif kind == "ties":
+            row = (g.integers(-3, 4, size=n) * 0.5).astype(np.float32)
+        elif kind == "ties3":
+            row = g.choice(np.array([-1.0, 0.25, 2.0], np.float32), size=n)
+        elif kind == "equal":
+            row = np.full(n, 0.75, np.float32)
+        else:
+            row = np.full(n, -np.inf, np.float32)
+            pos = g.choice(n, size=1000, replace=False)
+            row[pos] = g.standard_normal(1000).astype(np.float32)
+        logits[r, s:s + n] = row
+    out = run(idx, logits, starts, starts + lens, k)
+    for r in list(range(len(special))) + [50, 199]:
+        s, n = int(starts[r]), int(lens[r])
+        vals = logits[r, s:s + n].astype(np.float64)
+        check_topk(out[r], vals, np.zeros_like(vals), n, k, f"row {r} len {n} start {s}")

@@ -27,9 +27,11 @@ def _insert_both(idx, oracle, k_bits, slots, num_blocks, k_dev=None):
     return gcache.cpu().numpy(), ocache, errs.cpu().numpy(), bad
 
 
-def test_insert_random_bit_exact(idx, oracle):
+@pytest.mark.parametrize("n,num_blocks", [(1000, 20), (70000, 1300)])
+def test_insert_random_bit_exact(idx, oracle, n, num_blocks):
+    """Padding (-1), out-of-range and negative slots among valid ones, below
+    and above the size where a thread group takes four vectors."""
     g = wl.rng(201)
-    n, num_blocks = 1000, 20
     k = wl.normal_bf16(g, (n, 128), wl.outlier_channels(g))
     slots = g.permutation(num_blocks * 64)[:n].astype(np.int64)
     slots[g.choice(n, 50, replace=False)] = -1

@@ -121,13 +121,15 @@ idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, in
 }
 
 // Work items for the persistent paged kernels: each sequence's columns
-// [0, cols) are cut into items of whole 128-key tiles, about four items per
-// CTA over the batch (2..64 tiles each), and the grid holds as many CTAs as
-// fit on the device at once (or fewer when there are fewer items).
+// [0, cols) are cut into items of whole 128-key tiles, about twelve items per
+// CTA over the batch (2..64 tiles each; the static round-robin assignment
+// evens out sequences shorter than the block table over many small items),
+// and the grid holds as many CTAs as fit on the device at once (or fewer when
+// there are fewer items).
 void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh, int fixed_tiles = 0) {
   const int64_t ctas = (int64_t)sms * idx::paged_ctas_per_sm(nh);
   const int64_t tiles = (cols + 127) / 128;
-  int64_t per = (tiles * a.B + 4 * ctas - 1) / (4 * ctas);
+  int64_t per = (tiles * a.B + 12 * ctas - 1) / (12 * ctas);
   per = per < 2 ? 2 : (per > idx::kMaxTilesPerCta ? idx::kMaxTilesPerCta : per);
   if (fixed_tiles > 0) per = fixed_tiles;
   a.sms = sms;

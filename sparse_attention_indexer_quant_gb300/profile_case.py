@@ -5,6 +5,8 @@ CUDA-event time.  Cases:
     prefill T     causal single-sequence prefill of T tokens, H = 32:
                   mqa_logits, then topk_rows (k = 2048) on its logits
     decode        the batched decode workload: the fused paged logits + top-k
+    quant T       q-quant of a T-token prefill's query heads (H = 32), then
+                  the insert of its T keys into a paged cache
 
 Usage: python -m sparse_attention_indexer_quant_gb300.profile_case prefill 8192
 """
@@ -78,6 +80,18 @@ def main(argv):
         ms = _time(lambda: idx.paged_logits_topk(qv, qs, w, cache, bt, cl, p.next_n, p.H, 2048,
                                                  workspace=ws, out=out), flush, reps)
         print(f"batched decode: paged_logits_topk {ms * 1e3:.1f} us")
+    elif argv and argv[0] == "quant":
+        T = int(argv[1]) if len(argv) > 1 else 32768
+        p = wl.prefill(T=T)
+        q = _bf16(p.q, dev)
+        qv, qs = idx.quant_q(q)
+        ms = _time(lambda: idx.quant_q(q, out_vals=qv, out_scales=qs), flush, reps)
+        print(f"prefill T={T}: quant_q of {T * p.H} rows {ms * 1e3:.1f} us")
+        cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+        k = _bf16(p.k, dev)
+        slots = torch.from_numpy(p.slots).to(dev)
+        ms = _time(lambda: idx.quant_insert(k, slots, cache), flush, reps)
+        print(f"prefill T={T}: quant_insert of {k.shape[0]} keys {ms * 1e3:.1f} us")
     else:
         print(__doc__)
         return 2

@@ -63,6 +63,13 @@ def parse_args():
     ap.add_argument("--workload", default="batched_decode",
                     choices=sorted(WORKLOADS),
                     help="decode workload; the default is the headline configuration")
+    ap.add_argument("--case", nargs="+", metavar=("NAME", "T"),
+                    help="run one step of the path alone a few times for a profiler and "
+                         "print its median time: 'prefill T' (mqa_logits then topk_rows on "
+                         "a T-token causal prefill, H=32), 'decode' (the fused paged "
+                         "logits + top-k of the headline batch), 'quant T' (q-quant and "
+                         "insert of a T-token prefill)")
+    ap.add_argument("--reps", type=int, default=5, help="repetitions of a --case step")
     return ap.parse_args()
 
 
@@ -75,12 +82,16 @@ WORKLOADS = {
 }
 
 
-def make_workload(name, rank=0):
+def make_workload(name, rank=0, **sizes):
+    """Rank r's shard of a decode workload: the workload's recipe with its
+    seed moved by 1000 * r, so every rank owns different sequences and no
+    data crosses ranks (the decode path has no exchange step).  `sizes`
+    overrides the recipe's sizes (tests use small shards)."""
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     builder = getattr(wl, WORKLOADS[name][0])
     import inspect
     seed = inspect.signature(builder).parameters["seed"].default
-    return builder(seed=seed + 1000 * rank)
+    return builder(seed=seed + 1000 * rank, **sizes)
 
 
 def dist_info():
@@ -272,19 +283,6 @@ def run_ours(args, rank, world, local_rank):
     # tail, and host launch gaps would land inside the step); the fused call is
     # timed alone the same way for its roofline, and the step once more as
     # eager calls for reference.
-    def graph_of(fn):
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        torch.cuda.synchronize()
-        return g
-
     g_step = graph_of(lambda: (step(), fused()))
     g_fused = graph_of(fused)
     K = args.steps
@@ -366,6 +364,10 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_also:
         also = secondary_measurements(idx, dev, flush_l2, stream,
                                       decode=(p, cache, qv, qs, w, bt, cl))
+        also.update(insert_entries(idx, dev, flush_l2, stream))
+        for other in ("long_decode", "mixed_decode", "pr_ref"):
+            if other != args.workload:
+                also[other] = decode_workload_entry(other, idx, dev, flush_l2, stream)
 
     cpu = None
     if rank == 0:
@@ -435,6 +437,139 @@ def time_op(fn, flush_l2, stream, reps):
     return ts[len(ts) // 2]
 
 
+def fill_cache(idx, p, dev, rows=None, chunk=1 << 21):
+    """A poisoned cache with the given rows of a problem's keys inserted
+    (all of them by default), uploaded in bounded chunks."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+    rows = np.arange(p.total_tokens) if rows is None else np.asarray(rows)
+    for lo in range(0, len(rows), chunk):
+        r = rows[lo:lo + chunk]
+        idx.quant_insert(bf16_tensor(p.k[r], dev), torch.from_numpy(p.slots[r]).to(dev), cache)
+    return cache
+
+
+def graph_of(fn):
+    """A CUDA graph of fn's launches (captured after one warm call on a side
+    stream)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def decode_workload_entry(name, idx, dev, flush_l2, stream, reps=50, cpu_seconds=5.0):
+    """The fused decode call (paged logits + top-k) on another decode workload:
+    its CUDA-graph replay time with L2 flushed before each (median of reps),
+    its roofline fraction on the same algorithmic bytes as the headline, and
+    the oracle on a bounded sample of the same workload."""
+    import torch
+    import oracle
+    p = make_workload(name)
+    cache = fill_cache(idx, p, dev)
+    qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+    w = torch.from_numpy(p.weights).to(dev)
+    bt = torch.from_numpy(p.block_table).to(dev)
+    cl = torch.from_numpy(p.context_lens).to(dev)
+    ws = idx.new_paged_topk_workspace(p.B, p.next_n, p.block_table.shape[1], TOPK, dev)
+    out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
+    g = graph_of(lambda: idx.paged_logits_topk(qv, qs, w, cache, bt, cl, p.next_n, p.H, TOPK,
+                                               workspace=ws, out=out))
+    ms = time_op(g.replay, flush_l2, stream, reps)
+    hbm, src = peaks()
+    gbs = fused_algorithmic_bytes(p) / (ms * 1e-3) / 1e9
+    n_seq = max(1, min(p.B, oracle.num_threads() // p.next_n))
+    cpu = cpu_baseline(p, n_seq, cpu_seconds, max_steps=20)
+    del cache
+    return {"workload": name, "description": WORKLOADS[name][1],
+            "fused_ms": ms, "timing": f"median of {reps} CUDA-graph replays, L2 flushed before each",
+            "value": scored_tokens(p) / (ms * 1e-3), "unit": UNIT,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_source": f"{src} (hbm_gbs, burst)",
+                         "algorithmic_bytes_per_launch": fused_algorithmic_bytes(p)},
+            "cpu_baseline": cpu}
+
+
+def insert_entries(idx, dev, flush_l2, stream, reps=10):
+    """The insert where it streams: the headline batch's whole cache (every
+    context, 1.3 M keys) in one call, and the mixed step's insert batch (8 x
+    8192 chunked-prefill keys + 128 decode keys, with 5% padding rows)."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    hbm, _ = peaks()
+    res = {}
+    p = wl.batched_decode()
+    cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+    k = bf16_tensor(p.k, dev)
+    slots = torch.from_numpy(p.slots).to(dev)
+    ms = time_op(lambda: idx.quant_insert(k, slots, cache), flush_l2, stream, reps)
+    n = p.total_tokens
+    b = n * (256 + 8 + 68)
+    res["insert_batched_cache"] = {
+        "workload": f"the batched decode's whole cache: {n} bf16 keys in one call", "ms": ms,
+        "tokens_per_s": n / (ms * 1e-3), "gbs": b / (ms * 1e-3) / 1e9,
+        "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm}
+    del cache, k, slots
+    ib = wl.mixed_insert_batch()
+    cache = torch.from_numpy(wl.poisoned_cache(ib.num_blocks)).to(dev)
+    idx.quant_insert(bf16_tensor(ib.pre_k, dev), torch.from_numpy(ib.pre_slots).to(dev), cache)
+    k = bf16_tensor(ib.k, dev)
+    slots = torch.from_numpy(ib.slots).to(dev)
+    ms = time_op(lambda: idx.quant_insert(k, slots, cache), flush_l2, stream, reps)
+    real, pads = ib.real_rows, len(ib.slots) - ib.real_rows
+    b = real * (256 + 8 + 68) + pads * 8
+    res["insert_mixed_batch"] = {
+        "workload": f"the mixed step's insert batch: {real} keys + {pads} padding rows", "ms": ms,
+        "tokens_per_s": real / (ms * 1e-3), "gbs": b / (ms * 1e-3) / 1e9,
+        "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm}
+    return res
+
+
+def prefill_oracle_sample(p, qv, qs, kv, ks, logits_dev, n_rows=512, seed=4242):
+    """The oracle's prefill (logits and top-k) on a seeded sample of query rows
+    of the causal prefill, timed on the host cores, with the full-size time
+    extrapolated by valid (query, key) pairs; and a parity check of the GPU's
+    logits on those rows against the oracle (tolerance 1e-5 of the summed
+    magnitudes)."""
+    import oracle
+    g = np.random.default_rng(seed)
+    st, en = p.windows()
+    rows = np.sort(np.concatenate([g.choice(p.T, size=n_rows - 8, replace=False),
+                                   np.arange(8) * 37]))  # a few rows shorter than k
+    rows = np.unique(rows)
+    qv_h = qv.cpu().numpy().reshape(p.T, p.H, 64)[rows].reshape(-1, 64)
+    qs_h = qs.cpu().numpy().reshape(p.T, p.H, 4)[rows].reshape(-1, 4)
+    kv_h, ks_h = kv.cpu().numpy(), ks.cpu().numpy()
+    S = kv_h.shape[0]
+    t0 = time.perf_counter()
+    lg, mag = oracle.mqa_logits(qv_h, qs_h, p.H, kv_h, ks_h, p.weights[rows], st[rows], en[rows],
+                                ld=S)
+    oracle.topk_rows(np.nan_to_num(lg, nan=-np.inf), st[rows], en[rows], p.topk)
+    dt = time.perf_counter() - t0
+    pairs_s = int((en[rows].astype(np.int64) - st[rows]).sum())
+    pairs = int((en.astype(np.int64) - st).sum())
+    ok = True
+    for i, r in enumerate(rows):
+        a, b_ = int(st[r]), int(en[r])
+        got = logits_dev[int(r), a:b_].cpu().numpy().astype(np.float64)
+        ok &= bool((np.abs(got - lg[i, a:b_]) <= 1e-5 * mag[i, a:b_]).all())
+    return {"kind": "oracle", "sample": f"{len(rows)} seeded query rows of the {p.T}-row causal "
+                                        f"prefill ({pairs_s} of {pairs} valid pairs)",
+            "cores": oracle.num_threads(), "sample_seconds": dt,
+            "extrapolated_full_seconds": dt * pairs / pairs_s, "extrapolated": True,
+            "tflops": 2.0 * p.H * 128 * pairs_s / dt / 1e12,
+            "gpu_logits_match_oracle_on_sample": ok}
+
+
 def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
     """The other steps of the path, each timed alone with a flushed L2: insert,
     q-quant, gather, prefill logits and top-k on the 32K-token causal prefill
@@ -494,6 +629,7 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
     out = torch.empty((p.T, TOPK), dtype=torch.int32, device=dev)
     topk_ms = time_op(lambda: idx.topk_rows(logits, en_d, TOPK, row_start=st_d, out=out),
                       flush_l2, stream, reps)
+    pre_cpu = prefill_oracle_sample(p, qv, qs, kv, ks, logits)
     del logits
     tf = flops / (pre_ms * 1e-3) / 1e12
     res.update({
@@ -514,8 +650,44 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
                            "valid_pairs": pairs},
         "prefill_topk": {"workload": "32768 causal rows, k=2048", "ms": topk_ms,
                          "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9},
+        "prefill_cpu_baseline": pre_cpu,
     })
     return res
+
+
+def host_cpu_info():
+    """The host the CPU baseline runs on: logical CPUs, the ones this process
+    may use, the CPU model, and the OpenMP thread count the oracle runs with."""
+    import oracle
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                model = ln.split(":", 1)[1].strip()
+                if ln.startswith("Model name"):
+                    break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for ln in fh:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count()
+    threads = oracle.num_threads()
+    env = os.environ.get("OMP_NUM_THREADS")
+    why = (f"OMP_NUM_THREADS={env}" if env else
+           f"OpenMP's default: the {usable} CPUs in this process's affinity mask")
+    return {"nproc": os.cpu_count(), "usable_cpus": usable, "cpu_model": model,
+            "threads": threads, "threads_capped_by": why}
 
 
 def cpu_baseline(p, n_seq, min_seconds=10.0, max_steps=200):
@@ -548,7 +720,7 @@ def cpu_baseline(p, n_seq, min_seconds=10.0, max_steps=200):
             "kind": "oracle",
             "sample": f"{steps} decode steps over the first {n_seq} of {p.B} sequences "
                       f"({toks} key-tokens per step)",
-            "seconds": dt}
+            "seconds": dt, "host": host_cpu_info()}
 
 
 def run_reference(args, rank, world):
@@ -601,7 +773,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "config": workload_config(p, args.workload),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "host": host_cpu_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -639,8 +811,83 @@ def reduce_max(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def run_case(args):
+    """One step of the path alone, args.reps times with L2 flushed before each,
+    for a profiler to capture (ncu -k on the step's kernel); prints the median
+    CUDA-event time of each timed call."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import binding as idx
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    dev = torch.device("cuda")
+    idx.check_device(torch.cuda.current_device())
+    buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush():
+        buf.fill_(1)
+        torch.sum(buf, 0, dtype=torch.int64, out=sink)
+
+    stream = torch.cuda.current_stream()
+    name, rest = args.case[0], args.case[1:]
+    if name == "prefill":
+        T = int(rest[0]) if rest else 8192
+        p = wl.prefill(T=T)
+        S = int(p.tok_offsets[-1])
+        cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+        idx.quant_insert(bf16_tensor(p.k, dev), torch.from_numpy(p.slots).to(dev), cache)
+        kv, ks = idx.gather_k(cache, torch.from_numpy(p.block_table).to(dev),
+                              torch.from_numpy(p.new_lens.astype(np.int32)).to(dev),
+                              torch.zeros(1, dtype=torch.int64, device=dev), S)
+        qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+        w = torch.from_numpy(p.weights).to(dev)
+        st, en = p.windows()
+        st_d, en_d = torch.from_numpy(st).to(dev), torch.from_numpy(en).to(dev)
+        logits = torch.empty((p.T, S), dtype=torch.float32, device=dev)
+        out = torch.empty((p.T, TOPK), dtype=torch.int32, device=dev)
+        ms = time_op(lambda: idx.mqa_logits(qv, qs, w, kv, ks, st_d, en_d, p.H, out=logits),
+                     flush, stream, args.reps)
+        pairs = int((en.astype(np.int64) - st).sum())
+        print(f"prefill T={T}: mqa_logits {ms:.3f} ms "
+              f"({2.0 * p.H * 128 * pairs / (ms * 1e-3) / 1e12:.0f} TFLOP/s)")
+        ms = time_op(lambda: idx.topk_rows(logits, en_d, TOPK, row_start=st_d, out=out), flush,
+                     stream, args.reps)
+        print(f"prefill T={T}: topk_rows {ms:.3f} ms")
+    elif name == "decode":
+        p = wl.batched_decode()
+        cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+        idx.quant_insert(bf16_tensor(p.k, dev), torch.from_numpy(p.slots).to(dev), cache)
+        qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+        w = torch.from_numpy(p.weights).to(dev)
+        bt = torch.from_numpy(p.block_table).to(dev)
+        cl = torch.from_numpy(p.context_lens).to(dev)
+        ws = idx.new_paged_topk_workspace(p.B, p.next_n, p.block_table.shape[1], TOPK, dev)
+        out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
+        ms = time_op(lambda: idx.paged_logits_topk(qv, qs, w, cache, bt, cl, p.next_n, p.H, TOPK,
+                                                   workspace=ws, out=out), flush, stream,
+                     args.reps)
+        print(f"batched decode: paged_logits_topk {ms * 1e3:.1f} us")
+    elif name == "quant":
+        T = int(rest[0]) if rest else 32768
+        p = wl.prefill(T=T)
+        q = bf16_tensor(p.q, dev)
+        qv, qs = idx.quant_q(q)
+        ms = time_op(lambda: idx.quant_q(q, out_vals=qv, out_scales=qs), flush, stream,
+                     args.reps)
+        print(f"prefill T={T}: quant_q of {T * p.H} rows {ms * 1e3:.1f} us")
+        cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+        k = bf16_tensor(p.k, dev)
+        slots = torch.from_numpy(p.slots).to(dev)
+        ms = time_op(lambda: idx.quant_insert(k, slots, cache), flush, stream, args.reps)
+        print(f"prefill T={T}: quant_insert of {k.shape[0]} keys {ms * 1e3:.1f} us")
+    else:
+        raise SystemExit(f"unknown --case {name!r}")
+
+
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     rank, world, local_rank = dist_info()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)

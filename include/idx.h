@@ -214,14 +214,17 @@ IDX_API idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q
  *   Arguments as for idx_paged_logits_topk, without workspace/workspace_bytes.
  *   The scratch is a 32 MiB array inside the library: every GPU that loads the
  *   library reserves it until the process exits.  Its device address is looked
- *   up on the first call on each device (with that device current), so make
- *   that first call before any stream capture.
+ *   up on the first call in each CUDA context (the calling thread's current
+ *   one), so make that first call before any stream capture, and again after
+ *   a device reset (which ends the context).
  *   A batch whose idx_paged_logits_topk_workspace_bytes exceeds 32 MiB is
- *   rejected with IDX_ERR_INVALID_ARG (and a message on stderr); use
- *   idx_paged_logits_topk with a caller workspace for it.
+ *   rejected with IDX_ERR_INVALID_ARG (the reason is in
+ *   idx_last_error_detail()); use idx_paged_logits_topk with a caller
+ *   workspace for it.
  *   All calls share the one scratch array: calls that overlap on the GPU race.
- *   Nothing in the scratch needs clearing between calls: its work-item
- *   counter carries each call's generation.
+ *   Nothing in the scratch needs clearing between calls: the work-item counter
+ *   at its start carries each call's generation and is reset by the call's
+ *   select pass; the logits rows behind it are rewritten before being read.
  * ------------------------------------------------------------------------ */
 IDX_API idx_status idx_paged_logits_topk_noalloc(
     const uint8_t* q_vals, const uint8_t* q_scales, int32_t B, int32_t next_n, int32_t H,

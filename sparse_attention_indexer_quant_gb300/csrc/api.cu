@@ -17,8 +17,10 @@
 #include "paged_core.cuh"
 
 namespace {
-
 thread_local char g_detail[512] = "";
+}  // namespace
+
+namespace idx {
 
 idx_status fail(idx_status s, const char* fmt, ...) {
   va_list ap;
@@ -32,6 +34,13 @@ idx_status ok() {
   g_detail[0] = '\0';
   return IDX_OK;
 }
+
+}  // namespace idx
+
+namespace {
+
+using idx::fail;
+using idx::ok;
 
 // Generations of the fused call's work-item counter: distinct per call (of the
 // process), nonzero (a zero-filled workspace matches no call), below 2^40.
@@ -55,7 +64,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 rejected
 std::atomic<int> g_dev_sms[kMaxDevices];
 
-idx_status current_device_ok(int* sms_out) {
+idx_status current_device_ok_impl(int* sms_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return from_cuda(e, "cudaGetDevice");
@@ -142,6 +151,10 @@ void set_paged_chunking(idx::PagedArgs& a, int64_t cols, int sms, int nh, int fi
 
 }  // namespace
 
+namespace idx {
+idx_status current_device_ok(int* sms_out) { return current_device_ok_impl(sms_out); }
+}  // namespace idx
+
 extern "C" {
 
 int idx_version(void) { return 100; }
@@ -183,7 +196,7 @@ idx_status idx_quant_insert(const void* k_bf16, int64_t n_tokens, int64_t k_row_
   if (k_row_stride < 128 || (k_row_stride % 8) != 0)
     return fail(IDX_ERR_INVALID_ARG, "k_row_stride=%lld (>= 128, multiple of 8)",
                 (long long)k_row_stride);
-  idx_status s = current_device_ok(nullptr);
+  idx_status s = idx::current_device_ok(nullptr);
   if (s != IDX_OK) return s;
   if (n_tokens == 0) return ok();
   if (!k_bf16 || !slot_mapping || !kcache) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
@@ -198,7 +211,7 @@ idx_status idx_quant_q(const void* q_bf16, int64_t rows, uint8_t* q_vals, uint8_
                        idx_stream_t stream) {
   if (rows < 0 || rows > (int64_t)INT32_MAX * 16)
     return fail(IDX_ERR_INVALID_ARG, "rows=%lld", (long long)rows);
-  idx_status s = current_device_ok(nullptr);
+  idx_status s = idx::current_device_ok(nullptr);
   if (s != IDX_OK) return s;
   if (rows == 0) return ok();
   if (!q_bf16 || !q_vals || !q_scales) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
@@ -220,7 +233,7 @@ idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, 
   if (s != IDX_OK) return s;
   if (ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld", (long long)ld);
   int sms = 0;
-  s = current_device_ok(&sms);
+  s = idx::current_device_ok(&sms);
   if (s != IDX_OK) return s;
   if (B == 0) return ok();
   if (!logits) return fail(IDX_ERR_INVALID_ARG, "null logits");
@@ -254,7 +267,7 @@ idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int64_
   if (H != 32 && H != 64) return fail(IDX_ERR_INVALID_ARG, "H=%d not in {32,64}", H);
   if (S < 0 || S > (int64_t)INT32_MAX - 256) return fail(IDX_ERR_INVALID_ARG, "S=%lld", (long long)S);
   if (ld < S || ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld < S=%lld", (long long)ld, (long long)S);
-  idx_status s = current_device_ok(nullptr);
+  idx_status s = idx::current_device_ok(nullptr);
   if (s != IDX_OK) return s;
   if (T == 0 || S == 0) return ok();
   if (!q_vals || !q_scales || !k_vals || !k_scales || !weights || !row_start || !row_end || !logits)
@@ -296,7 +309,7 @@ idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const in
   if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
   if (ld <= 0) return fail(IDX_ERR_INVALID_ARG, "ld=%lld", (long long)ld);
   int sms = 0;
-  idx_status s = current_device_ok(&sms);
+  idx_status s = idx::current_device_ok(&sms);
   if (s != IDX_OK) return s;
   if (rows == 0) return ok();
   if (!logits || !row_end || !out_idx) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
@@ -323,14 +336,14 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
                                     block_table, max_blocks, context_lens, weights);
   if (s != IDX_OK) return s;
   if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
-  s = current_device_ok(nullptr);
+  s = idx::current_device_ok(nullptr);
   if (s != IDX_OK) return s;
   if (B == 0) return ok();
   if (!out_idx) return fail(IDX_ERR_INVALID_ARG, "null out_idx");
   if ((int64_t)B * next_n > 65535)
     return fail(IDX_ERR_INVALID_ARG, "B*next_n=%d above 65535", B * next_n);
   int sms = 0;
-  if ((s = current_device_ok(&sms)) != IDX_OK) return s;
+  if ((s = idx::current_device_ok(&sms)) != IDX_OK) return s;
   const size_t need = idx::paged_topk_workspace_bytes(B, next_n, max_blocks, k);
   if (workspace_bytes < need || workspace == nullptr)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
@@ -376,7 +389,7 @@ idx_status idx_gather_k(const uint8_t* kcache, int64_t num_blocks, int32_t page_
   if (max_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks=%d", max_blocks);
   if (num_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "num_blocks=%lld", (long long)num_blocks);
   if (out_rows < 0) return fail(IDX_ERR_INVALID_ARG, "out_rows=%lld", (long long)out_rows);
-  idx_status s = current_device_ok(nullptr);
+  idx_status s = idx::current_device_ok(nullptr);
   if (s != IDX_OK) return s;
   if (B == 0) return ok();
   if (!kcache || !block_table || !seq_lens || !out_offsets || !k_vals || !k_scales)

@@ -9,6 +9,14 @@
 
 namespace idx {
 
+// Records a detail message for idx_last_error_detail() (this host thread) and
+// returns s; ok() clears it and returns IDX_OK.
+idx_status fail(idx_status s, const char* fmt, ...);
+idx_status ok();
+// The fail-closed device gate of every entry point, applied to the current
+// device (cached per device); *sms_out gets its SM count.
+idx_status current_device_ok(int* sms_out);
+
 cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_stride,
                                 const int64_t* slots, uint8_t* cache, int64_t num_blocks,
                                 idx_device_errors* errors, cudaStream_t stream);

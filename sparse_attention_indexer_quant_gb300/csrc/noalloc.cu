@@ -12,18 +12,22 @@
 // Costs and rules:
 //   - the array below is reserved on every GPU that loads this part of the
 //     library and stays reserved until the process exits;
-//   - its device address is looked up on the first call on each device (with
-//     that device current); make that first call before any stream capture;
+//   - its device address is looked up on the first call in each CUDA context
+//     (the current one of the calling thread) and kept for later calls in
+//     that context; make that first call before any stream capture;
 //   - all calls share the one array, so calls that overlap on the GPU (on
 //     different streams without ordering) race and give wrong results;
-//   - the parts of the scratch that must start at zero are cleared by every
-//     call; the rest keeps the previous call's contents.
+//   - nothing has to be cleared between calls: the work-item counter at the
+//     start of the scratch carries each call's generation and the select pass
+//     resets it at the end of every call; the logits rows behind it are
+//     rewritten by every call before they are read.
+#include <cuda.h>
 #include <cuda_runtime.h>
-#include <stdio.h>
 
 #include <mutex>
 
 #include "idx.h"
+#include "launch.h"
 
 namespace {
 
@@ -31,11 +35,30 @@ constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;  // 32 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// The scratch address per CUDA context: a module global has one address per
+// context, so a context made after a device reset (or a second context on the
+// same device) gets its own lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-thread_local char g_msg[256] = "";
+CtxGetCurrentFn ctx_get_current_fn() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+CUcontext g_ctx[kMaxContexts] = {};
+void* g_scratch_addr[kMaxContexts] = {};
+int g_n_ctx = 0;
 
 }  // namespace
 
@@ -46,31 +69,39 @@ extern "C" IDX_API idx_status idx_paged_logits_topk_noalloc(
     int32_t* out_idx, idx_device_errors* errors, idx_stream_t stream) {
   const size_t need =
       idx_paged_logits_topk_workspace_bytes(B, next_n, max_blocks, page_size, k);
-  if (need > kNoAllocScratchBytes) {
-    snprintf(g_msg, sizeof g_msg,
-             "this batch needs %zu bytes of scratch; the built-in scratch holds %zu "
-             "(use idx_paged_logits_topk with a caller workspace)",
-             need, kNoAllocScratchBytes);
-    fprintf(stderr, "idx_paged_logits_topk_noalloc: %s\n", g_msg);
-    return IDX_ERR_INVALID_ARG;
-  }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return IDX_ERR_CUDA;
+  if (need > kNoAllocScratchBytes)
+    return idx::fail(IDX_ERR_INVALID_ARG,
+                     "this batch needs %zu bytes of scratch; the built-in scratch holds %zu "
+                     "(use idx_paged_logits_topk with a caller workspace)",
+                     need, kNoAllocScratchBytes);
+  // the device gate first: on any other device the library has no image, so
+  // the symbol lookup below could not succeed
+  idx_status s = idx::current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+    return idx::fail(IDX_ERR_CUDA, "no current CUDA context");
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    for (int i = 0; i < g_n_ctx; ++i)
+      if (g_ctx[i] == ctx) scratch = g_scratch_addr[i];
+    if (scratch == nullptr) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || p == nullptr) {
-        fprintf(stderr, "idx_paged_logits_topk_noalloc: cudaGetSymbolAddress: %s\n",
-                cudaGetErrorString(e));
-        return IDX_ERR_CUDA;
+        (void)cudaGetLastError();  // leave no pending error behind
+        return idx::fail(IDX_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch: %s",
+                         cudaGetErrorString(e));
       }
-      g_scratch_addr[dev] = p;
+      if (g_n_ctx == kMaxContexts)
+        return idx::fail(IDX_ERR_CUDA, "more than %d CUDA contexts", kMaxContexts);
+      g_ctx[g_n_ctx] = ctx;
+      g_scratch_addr[g_n_ctx] = p;
+      ++g_n_ctx;
+      scratch = p;
     }
-    scratch = g_scratch_addr[dev];
   }
   return idx_paged_logits_topk(q_vals, q_scales, B, next_n, H, kcache, num_blocks, page_size,
                                block_table, max_blocks, context_lens, weights, k, out_idx,

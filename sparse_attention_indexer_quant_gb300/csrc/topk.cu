@@ -4,8 +4,8 @@
 //   - up to one row per SM: one thread-block cluster of P CTAs per row running
 //     cluster_select_row (select_row.cuh), so that a few long rows use the
 //     whole GPU;
-//   - more rows: one 512-thread CTA per row running row_topk (topk_row.cuh),
-//     two CTAs per SM, for throughput over many rows.
+//   - more rows: one 256-thread CTA per row running row_topk (topk_row.cuh),
+//     four CTAs per SM, for throughput over many rows.
 #include "common.cuh"
 #include "launch.h"
 #include "select_row.cuh"

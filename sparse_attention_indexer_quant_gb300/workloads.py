@@ -243,7 +243,8 @@ class PrefillProblem:
 
 
 def make_prefill(name: str, seed: int, prefix_lens, new_lens, H: int,
-                 page_size: int = PAGE_SIZE, topk: int = TOPK) -> PrefillProblem:
+                 page_size: int = PAGE_SIZE, topk: int = TOPK,
+                 with_queries: bool = True) -> PrefillProblem:
     g = rng(seed)
     P = np.asarray(prefix_lens, np.int32)
     N = np.asarray(new_lens, np.int32)
@@ -256,8 +257,14 @@ def make_prefill(name: str, seed: int, prefix_lens, new_lens, H: int,
     for b in range(len(P)):
         slots[offs[b]:offs[b + 1]] = slots_of(bt, b, np.arange(lens[b]), page_size)
     T = int(N.sum())
-    q = normal_bf16(g, (T, H, HEAD_DIM))
-    w = head_weights(g, T, H)
+    # the queries are drawn after the keys, so leaving them out (an insert
+    # needs only the keys) changes nothing else
+    if with_queries:
+        q = normal_bf16(g, (T, H, HEAD_DIM))
+        w = head_weights(g, T, H)
+    else:
+        q = np.zeros((0, H, HEAD_DIM), np.uint16)
+        w = np.zeros((0, H), np.float32)
     return PrefillProblem(name, H, page_size, P, N, bt, num_blocks, k, offs, slots, q, w, topk)
 
 
@@ -267,12 +274,12 @@ def prefill(seed: int = 1004, T: int = 32768, H: int = 32) -> PrefillProblem:
 
 
 def mixed_prefill_part(seed: int = 1005, B: int = 8, new: int = 8192, max_prefix: int = 65536,
-                       H: int = 32) -> PrefillProblem:
+                       H: int = 32, with_queries: bool = True) -> PrefillProblem:
     """The chunked-prefill half of the mixed batch: B sequences with prefixes
     uniform in [0, max_prefix], each adding ``new`` tokens."""
     g = rng(seed + 104729)
     P = g.integers(0, max_prefix + 1, size=B)
-    return make_prefill("mixed_prefill", seed, P, [new] * B, H)
+    return make_prefill("mixed_prefill", seed, P, [new] * B, H, with_queries=with_queries)
 
 
 def mixed_decode_part(seed: int = 1006, B: int = 128, lo: int = 1024, hi: int = 131072,
@@ -297,3 +304,59 @@ def with_padding(g: np.random.Generator, slots: np.ndarray, frac: float = 0.05):
     real_pos = np.nonzero(~is_pad)[0]
     out[real_pos] = slots
     return out, real_pos
+
+
+@dataclasses.dataclass
+class InsertBatch:
+    """One insert batch into a paged cache, with the keys the cache must
+    already hold (``pre_k`` at ``pre_slots``).  ``slots`` holds -1 for the
+    padding rows; their keys are drawn like the others but never written."""
+    name: str
+    num_blocks: int
+    pre_k: np.ndarray             # uint16 [n_pre, 128]
+    pre_slots: np.ndarray         # int64 [n_pre]
+    k: np.ndarray                 # uint16 [n, 128]
+    slots: np.ndarray             # int64 [n]
+
+    @property
+    def real_rows(self) -> int:
+        return int((self.slots >= 0).sum())
+
+
+def mixed_insert_batch(seed: int = 1007, frac_pad: float = 0.05, prefill_seed: int = 1005,
+                       decode_seed: int = 1006, B_prefill: int = 8, new: int = 8192,
+                       max_prefix: int = 65536, B_decode: int = 128, lo: int = 1024,
+                       hi: int = 131072) -> InsertBatch:
+    """The insert batch of the mixed chunked-prefill + decode step: the new
+    tokens of the chunked prefills (each sequence's ``new`` tokens after its
+    cached prefix) and one new token per decode sequence (at the end of its
+    context), plus round(frac_pad * n) padding rows (slot -1) at seeded
+    positions.  Both halves share one cache: the prefill half's pages first,
+    then the decode half's (the same page pools and block tables as
+    ``mixed_prefill_part`` and ``mixed_decode_part``).  The prefills' cached
+    prefixes are the keys the cache holds before the batch.  The decode
+    tokens' keys are fresh N(0,1) rows: the decode contexts themselves are
+    not needed for an insert."""
+    pp = mixed_prefill_part(seed=prefill_seed, B=B_prefill, new=new, max_prefix=max_prefix,
+                            with_queries=False)
+    gl = rng(decode_seed + 15485863)
+    lens = gl.integers(lo, hi + 1, size=B_decode)
+    dbt, d_blocks = shuffled_block_table(rng(decode_seed), lens)
+    pre_rows, new_rows = [], []
+    for b in range(pp.B):
+        base, P = int(pp.tok_offsets[b]), int(pp.prefix_lens[b])
+        pre_rows.append(np.arange(base, base + P))
+        new_rows.append(np.arange(base + P, int(pp.tok_offsets[b + 1])))
+    pre_rows = np.concatenate(pre_rows)
+    new_rows = np.concatenate(new_rows)
+    d_slots = np.array([slots_of(dbt, b, [int(lens[b]) - 1])[0] for b in range(B_decode)],
+                       np.int64) + pp.num_blocks * PAGE_SIZE
+    g = rng(seed)
+    d_k = normal_bf16(g, (B_decode, HEAD_DIM))
+    real_slots = np.concatenate([pp.slots[new_rows], d_slots])
+    real_k = np.concatenate([pp.k[new_rows], d_k])
+    slots, real_pos = with_padding(g, real_slots, frac_pad)
+    k = normal_bf16(g, (len(slots), HEAD_DIM))
+    k[real_pos] = real_k
+    return InsertBatch("mixed_insert", pp.num_blocks + d_blocks, pp.k[pre_rows],
+                       pp.slots[pre_rows], k, slots)

@@ -80,6 +80,14 @@ def _load():
         lib.oracle_topk_rows.restype = None
         lib.oracle_gather_k.argtypes = [P, i32, P, i32, P, P, i32, P, P]
         lib.oracle_gather_k.restype = None
+        lib.oracle_quant_vec128_f32.argtypes = [P, P, P]
+        lib.oracle_quant_vec128_f32.restype = None
+        lib.oracle_rope_quant_q.argtypes = [P, P, i64, i32, P, P, i32, P, P, P]
+        lib.oracle_rope_quant_q.restype = None
+        lib.oracle_kpool_compress.argtypes = [P, P, P, P, i64, i32, P, P]
+        lib.oracle_kpool_compress.restype = None
+        lib.oracle_kpool_insert.argtypes = [P, P, i64, i32, P, i64, i32]
+        lib.oracle_kpool_insert.restype = i64
         _lib = lib
         return lib
 
@@ -225,3 +233,65 @@ def gather_k(cache, block_table, seq_lens, out_offsets, total_rows, page_size=64
     _load().oracle_gather_k(_ptr(c), int(page_size), _ptr(bt), int(bt.shape[1]), _ptr(sl),
                             _ptr(oo), int(sl.shape[0]), _ptr(v), _ptr(s))
     return v, s
+
+
+# ---------------------------------------------------------------- next steps
+
+def quant_vec128_f32(x):
+    """One fp32 vector of 128 -> (vals[64] u8, scales[4] u8), the same rules
+    applied to the exact fp32 values."""
+    xf = _c(x, np.float32).reshape(HEAD_DIM)
+    v = np.zeros(VAL_BYTES, np.uint8)
+    s = np.zeros(SCALE_BYTES, np.uint8)
+    _load().oracle_quant_vec128_f32(_ptr(xf), _ptr(v), _ptr(s))
+    return v, s
+
+
+def rope_quant_q(q_bf16_bits, positions, cos, sin, rot_dim: int):
+    """Rotary embedding of query heads then MXFP4 quantisation.
+    q [T, H, 128] bf16 bits; positions [T] rows of the tables; cos, sin
+    [num_pos, rot_dim / 2] fp32.  The first rot_dim dimensions rotate in pairs
+    (2i, 2i+1) by table column i, in fp32 with the order stated in oracle.c.
+    Returns (vals [T*H, 64], scales [T*H, 4], rotated fp32 [T*H, 128])."""
+    q = _c(q_bf16_bits, np.uint16)
+    T, H = q.shape[0], q.shape[1]
+    pos = _c(positions, np.int32)
+    cs = _c(cos, np.float32)
+    sn = _c(sin, np.float32)
+    assert rot_dim % 2 == 0 and 0 <= rot_dim <= HEAD_DIM
+    assert cs.shape == sn.shape and (rot_dim == 0 or cs.shape[1] == rot_dim // 2)
+    assert len(pos) == T and (T == 0 or (pos.min() >= 0 and pos.max() < max(cs.shape[0], 1)))
+    v = np.zeros((T * H, VAL_BYTES), np.uint8)
+    s = np.zeros((T * H, SCALE_BYTES), np.uint8)
+    r = np.zeros((T * H, HEAD_DIM), np.float32)
+    _load().oracle_rope_quant_q(_ptr(q), _ptr(pos), T, H, _ptr(cs), _ptr(sn), rot_dim, _ptr(v),
+                                _ptr(s), _ptr(r))
+    return v, s, r
+
+
+def kpool_compress(k_bf16_bits, gate, ape, slot_mapping, pool: int):
+    """The pooled key of every row that the K-pool insert writes, in fp64:
+    kc[p, d] = sum_j softmax_j(gate[p-P+1+j, d] + ape[j, d]) * k[p-P+1+j, d]
+    for rows p with slot >= 0 and p >= P - 1 (NaN elsewhere), and beside it the
+    tolerance scale mag[p, d] = sum_j w_j |k[p-P+1+j, d]|."""
+    k = _c(k_bf16_bits, np.uint16).reshape(-1, HEAD_DIM)
+    n = k.shape[0]
+    g = _c(gate, np.float32).reshape(n, HEAD_DIM)
+    a = _c(ape, np.float32).reshape(pool, HEAD_DIM)
+    sl = _c(slot_mapping, np.int64).reshape(n)
+    kc = np.zeros((n, HEAD_DIM), np.float64)
+    mag = np.zeros((n, HEAD_DIM), np.float64)
+    _load().oracle_kpool_compress(_ptr(k), _ptr(g), _ptr(a), _ptr(sl), n, int(pool), _ptr(kc),
+                                  _ptr(mag))
+    return kc, mag
+
+
+def kpool_insert(kc32, slot_mapping, pool: int, cache, page_size: int = 64):
+    """The write step of the K-pool insert: every row p with slot >= 0 and
+    p >= P - 1 (and n >= P) stores the MXFP4 encoding of its pooled fp32
+    vector kc32[p] at its slot.  Returns the count of out-of-range slots."""
+    kc = _c(kc32, np.float32).reshape(-1, HEAD_DIM)
+    sl = _c(slot_mapping, np.int64).reshape(-1)
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
+    return int(_load().oracle_kpool_insert(_ptr(kc), _ptr(sl), len(sl), int(pool), _ptr(cache),
+                                           cache.shape[0], page_size))

@@ -292,3 +292,127 @@ void oracle_gather_k(const uint8_t* cache, int32_t page_size, const int32_t* blo
     }
   }
 }
+
+/* ------------------------------------------------------------------------
+ * Quantisation of an fp32 vector of 128 (the rounded result of an fp32
+ * computation, e.g. a rotated query or a pooled key): the same scale, code and
+ * packing rules as oracle_quant_vec128, applied to the exact fp32 values. */
+void oracle_quant_vec128_f32(const float* xf, uint8_t* vals, uint8_t* scales) {
+  double x[D_HEAD];
+  for (int d = 0; d < D_HEAD; ++d) x[d] = (double)xf[d];
+  uint8_t codes[D_HEAD];
+  for (int b = 0; b < D_HEAD / BLOCK; ++b) {
+    uint8_t s = oracle_ue8m0_scale(x + b * BLOCK, BLOCK);
+    scales[b] = s;
+    for (int i = 0; i < BLOCK; ++i)
+      codes[b * BLOCK + i] = oracle_e2m1_code(ldexp(x[b * BLOCK + i], 127 - (int)s));
+  }
+  for (int i = 0; i < VAL_BYTES; ++i)
+    vals[i] = (uint8_t)((codes[2 * i + 1] << 4) | codes[2 * i]); /* element 2i low */
+}
+
+/* ------------------------------------------------------------------------
+ * Rotary position embedding of query heads, then MXFP4 quantisation
+ * ([PR-48558] "Notes": a fused q-rope + MXFP4 q-quant).  The pages give no
+ * rotary parameters, so the caller passes the table:
+ *   q      [T, H, 128] bf16; pos [T] row of the table for token t;
+ *   cs, sn [num_pos, rot_dim / 2] fp32 cosines and sines.
+ * Reading: the first rot_dim dimensions (even, <= 128) are rotated in
+ * interleaved pairs (2i, 2i+1) by the angle of table column i; the other
+ * dimensions pass through.  The rotation is an fp32 computation whose result
+ * is then quantised, so the rounding that decides the codes is fixed here in
+ * fp32 with one stated order:
+ *   x' = fmaf(x, c, -(y * s)),  y' = fmaf(x, s, y * c)
+ * (each product y*s, y*c rounded to fp32 first, then one fused multiply-add).
+ * out_f32 (optional) receives the rotated values. */
+void oracle_rope_quant_q(const uint16_t* q, const int32_t* pos, int64_t T, int32_t H,
+                         const float* cs, const float* sn, int32_t rot_dim, uint8_t* vals,
+                         uint8_t* scales, float* out_f32) {
+  const int32_t half = rot_dim / 2;
+  for (int64_t t = 0; t < T; ++t) {
+    const float* c_row = cs + (int64_t)pos[t] * half;
+    const float* s_row = sn + (int64_t)pos[t] * half;
+    for (int32_t h = 0; h < H; ++h) {
+      const int64_t r = t * H + h;
+      float x[D_HEAD];
+      for (int d = 0; d < D_HEAD; ++d) x[d] = (float)oracle_bf16_to_double(q[r * D_HEAD + d]);
+      for (int32_t i = 0; i < half; ++i) {
+        const float a = x[2 * i], b = x[2 * i + 1], c = c_row[i], s = s_row[i];
+        const float bs = b * s, bc = b * c;
+        x[2 * i] = fmaf(a, c, -bs);
+        x[2 * i + 1] = fmaf(a, s, bc);
+      }
+      if (out_f32) memcpy(out_f32 + r * D_HEAD, x, sizeof x);
+      oracle_quant_vec128_f32(x, vals + r * VAL_BYTES, scales + r * SCALE_BYTES);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------
+ * K-pool compressed insert ([SPARSE-IDX] _kpool_compress_insert).
+ * The masking rule is the page's: with n rows and pool size P, row p is a
+ * pool-completion candidate; it is written iff slot[p] >= 0 and p >= P - 1
+ * (a valid slot at p < P - 1 belongs to a pool that started before the batch
+ * and is dropped); nothing is written when n < P.  Pool p covers rows
+ * p - P + 1 .. p.
+ * The pooling arithmetic is not given by the pages; reading: per dimension d,
+ * the pool's rows are weighted by a softmax over the pool of
+ * gate[row, d] + ape[j, d] (j = position of the row within the pool) and
+ * summed:  kc[d] = sum_j softmax_j(gate + ape) * k[row_j, d].
+ *
+ * oracle_kpool_compress: kc for every candidate row in fp64 (rows that are not
+ * written get NaN), and beside it mag[p, d] = sum_j w_j |k[row_j, d]| (the
+ * scale of the comparison tolerance).  gate [n, 128] fp32, ape [P, 128] fp32,
+ * k [n, 128] bf16. */
+void oracle_kpool_compress(const uint16_t* k, const float* gate, const float* ape,
+                           const int64_t* slots, int64_t n, int32_t P, double* kc, double* mag) {
+  double* z = (double*)malloc(sizeof(double) * (size_t)(P > 0 ? P : 1));
+  for (int64_t p = 0; p < n; ++p) {
+    const int write = (n >= P) && slots[p] >= 0 && p >= P - 1;
+    const int64_t r0 = p - P + 1; /* the pool's first row */
+    for (int d = 0; d < D_HEAD; ++d) {
+      if (!write) {
+        kc[p * D_HEAD + d] = NAN;
+        mag[p * D_HEAD + d] = NAN;
+        continue;
+      }
+      double m = -INFINITY;
+      for (int32_t j = 0; j < P; ++j) {
+        z[j] = (double)gate[(r0 + j) * D_HEAD + d] + (double)ape[(int64_t)j * D_HEAD + d];
+        if (z[j] > m) m = z[j];
+      }
+      double den = 0.0, num = 0.0, am = 0.0;
+      for (int32_t j = 0; j < P; ++j) {
+        const double e = exp(z[j] - m);
+        const double kv = oracle_bf16_to_double(k[(r0 + j) * D_HEAD + d]);
+        den += e;
+        num += e * kv;
+        am += e * fabs(kv);
+      }
+      kc[p * D_HEAD + d] = num / den;
+      mag[p * D_HEAD + d] = am / den;
+    }
+  }
+  free(z);
+}
+
+/* The write step of the K-pool insert: the pooled vector of every written row
+ * p (kc32 [n, 128], the fp32 values that are quantised; other rows are not
+ * read) is quantised like a key and stored at slot[p] of the paged cache.
+ * Slots outside [0, num_blocks * page_size) are skipped and counted. */
+int64_t oracle_kpool_insert(const float* kc32, const int64_t* slots, int64_t n, int32_t P,
+                            uint8_t* cache, int64_t num_blocks, int32_t page_size) {
+  int64_t bad = 0;
+  if (n < P) return 0;
+  const int64_t page_bytes = (int64_t)page_size * (VAL_BYTES + SCALE_BYTES);
+  for (int64_t p = P - 1; p < n; ++p) {
+    const int64_t slot = slots[p];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * (int64_t)page_size) { ++bad; continue; }
+    const int64_t page = slot / page_size, off = slot % page_size;
+    oracle_quant_vec128_f32(kc32 + p * D_HEAD, cache + page * page_bytes + off * VAL_BYTES,
+                            cache + page * page_bytes + (int64_t)page_size * VAL_BYTES +
+                                off * SCALE_BYTES);
+  }
+  return bad;
+}

@@ -10,7 +10,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PIN_TESTS = [os.path.join(ROOT, "tests", f) for f in
-             ("test_oracle_quant.py", "test_oracle_logits.py")]
+             ("test_oracle_quant.py", "test_oracle_logits.py", "test_oracle_next.py")]
 
 # (name, original text, mutated text): each must occur exactly once.
 MUTATIONS = [
@@ -39,6 +39,24 @@ MUTATIONS = [
     ("topk_not_relative", "tmp[i].i = i; }", "tmp[i].i = i + st; }"),
     ("q_head_stride", "oracle_dequant_vec128(q_vals + (t * H + h) * VAL_BYTES, q_scales + (t * H + h) * SCALE_BYTES,",
      "oracle_dequant_vec128(q_vals + (t + h) * VAL_BYTES, q_scales + (t + h) * SCALE_BYTES,"),
+    ("rope_sign", "x[2 * i] = fmaf(a, c, -bs);", "x[2 * i] = fmaf(a, c, bs);"),
+    ("rope_sin_for_cos", "x[2 * i + 1] = fmaf(a, s, bc);", "x[2 * i + 1] = fmaf(a, c, bc);"),
+    ("rope_half_split_pairs", "const float a = x[2 * i], b = x[2 * i + 1],",
+     "const float a = x[i], b = x[i + half],"),
+    ("rope_token_not_position", "const float* c_row = cs + (int64_t)pos[t] * half;",
+     "const float* c_row = cs + (int64_t)t * half;"),
+    ("kpool_mask_late", "const int write = (n >= P) && slots[p] >= 0 && p >= P - 1;",
+     "const int write = (n >= P) && slots[p] >= 0 && p >= P;"),
+    ("kpool_window_shift", "const int64_t r0 = p - P + 1; /* the pool's first row */",
+     "const int64_t r0 = p - P + 2; /* the pool's first row */"),
+    ("kpool_ape_reversed", "+ (double)ape[(int64_t)j * D_HEAD + d];",
+     "+ (double)ape[(int64_t)(P - 1 - j) * D_HEAD + d];"),
+    ("kpool_mag_abs", "am += e * fabs(kv);", "am += e * kv;"),
+    ("quant_f32_nibbles", "vals[i] = (uint8_t)((codes[2 * i + 1] << 4) | codes[2 * i]); /* element 2i low */",
+     "vals[i] = (uint8_t)((codes[2 * i] << 4) | codes[2 * i + 1]);"),
+    ("kpool_insert_from_zero", "for (int64_t p = P - 1; p < n; ++p) {", "for (int64_t p = 0; p < n; ++p) {"),
+    ("quant_f32_scale_block", "uint8_t s = oracle_ue8m0_scale(x + b * BLOCK, BLOCK);\n    scales[b] = s;\n    for (int i = 0; i < BLOCK; ++i)\n      codes[b * BLOCK + i] = oracle_e2m1_code(ldexp(x[b * BLOCK + i], 127 - (int)s));",
+     "uint8_t s = oracle_ue8m0_scale(x, BLOCK);\n    scales[b] = s;\n    for (int i = 0; i < BLOCK; ++i)\n      codes[b * BLOCK + i] = oracle_e2m1_code(ldexp(x[b * BLOCK + i], 127 - (int)s));"),
 ]
 
 

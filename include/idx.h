@@ -126,6 +126,56 @@ IDX_API idx_status idx_quant_q(const void* q_bf16, int64_t rows, uint8_t* q_vals
                        idx_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * idx_rope_quant_q -- rotary position embedding of the query heads fused with
+ * their MXFP4 quantisation (PR #48558, "Notes": a fused q-rope + MXFP4 q-quant
+ * kernel could follow the PyTorch q-quant).  The pages give no rotary
+ * parameters; the caller passes the table.
+ *   q_bf16     [T, H, 128] bf16, contiguous, 16-byte aligned.
+ *   positions  [T] int32: the table row of token t.  When rot_dim > 0, a token
+ *              whose position is outside [0, num_pos) is skipped (its rows are
+ *              not written) and counted in errors->bad_inputs; with rot_dim = 0
+ *              positions are not read (may be any pointer, even NULL).
+ *   cos_table, sin_table [num_pos, rot_dim / 2] fp32: cosine and sine of the
+ *              angle of pair i at each position (may be NULL when rot_dim = 0).
+ *   rot_dim    even, 0..128: dimensions [0, rot_dim) turn in pairs (2i, 2i+1):
+ *              x' = x cos - y sin, y' = x sin + y cos, in fp32 with the products
+ *              y sin and y cos rounded first and one fused multiply-add each;
+ *              the other dimensions pass through.
+ *   q_vals / q_scales [T*H, 64] / [T*H, 4] out, as idx_quant_q (row t*H + h).
+ * ------------------------------------------------------------------------ */
+IDX_API idx_status idx_rope_quant_q(const void* q_bf16, int64_t T, int32_t H,
+                            const int32_t* positions, const float* cos_table,
+                            const float* sin_table, int32_t num_pos, int32_t rot_dim,
+                            uint8_t* q_vals, uint8_t* q_scales, idx_device_errors* errors,
+                            idx_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * idx_kpool_insert -- K-pool compressed insert (sparse_indexer docs,
+ * _kpool_compress_insert): pools of kpool consecutive keys become one MXFP4
+ * key, written at pool-granular slots, masked in the kernel (no compaction,
+ * no synchronisation).
+ *   k_bf16        [n, 128] bf16 keys of the batch in token order, contiguous.
+ *   gate          [n, 128] fp32 gate scores; ape [kpool, 128] fp32 position terms.
+ *   slot_mapping  [n] int64, pool-granular: row p completes a pool, and is
+ *                 written, iff slot[p] >= 0 and p >= kpool - 1 (a valid slot
+ *                 earlier belongs to a pool that began before the batch); a
+ *                 batch with n < kpool writes nothing.  Slots past the cache are
+ *                 skipped and counted.  Pool chunks start pool-aligned.
+ *   Written row p: kc[d] = sum_j softmax_j(gate[p-kpool+1+j, d] + ape[j, d])
+ *                 * k[p-kpool+1+j, d] over j < kpool (fp32; the pages fix the
+ *                 masking, this library reads the pooling as a softmax of gate
+ *                 plus position term), quantised as a key and stored at slot[p].
+ *   kcache        paged cache as for idx_quant_insert.
+ *   pooled        [n, 128] fp32 out, optional (NULL): kc of the written rows;
+ *                 other rows are not touched.
+ *   1 <= kpool <= 128.
+ * ------------------------------------------------------------------------ */
+IDX_API idx_status idx_kpool_insert(const void* k_bf16, const float* gate, const float* ape,
+                            const int64_t* slot_mapping, int64_t n, int32_t kpool,
+                            uint8_t* kcache, int64_t num_blocks, int32_t page_size,
+                            float* pooled, idx_device_errors* errors, idx_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * idx_paged_mqa_logits -- decode logits through block tables (sparse_indexer
  * docs: paged_mqa_logits; PR #48558 "Notes": the paged MQA-logits reader).
  *   q_vals/q_scales  [B*next_n*H, 64] / [B*next_n*H, 4]: query row r = b*next_n + j,
@@ -166,6 +216,31 @@ IDX_API idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales
                           const float* weights, const int32_t* row_start,
                           const int32_t* row_end, float* logits, int64_t ld, int clean,
                           idx_device_errors* errors, idx_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * idx_mqa_logits_topk -- idx_mqa_logits followed by top-k of every row
+ * (sparse_indexer docs: mqa_logits then top_k_per_row) without a logits
+ * tensor: the scoring kernel keeps, per row, a threshold that only grows (the
+ * k-th largest of the logits admitted so far, to within a histogram bin) and
+ * appends only the logits that reach it, with their positions, to the row's
+ * candidate list; a second kernel selects the k largest of each list.
+ *   Arguments as for idx_mqa_logits (without logits/ld/clean) and
+ *   idx_topk_rows: out_idx [T, k] int32 holds positions relative to
+ *   row_start[t], in no particular order, -1 after the last valid one.
+ *   workspace  at least idx_mqa_logits_topk_workspace_bytes(T, S, k) bytes,
+ *              256-byte aligned, no initialisation: per row a list of up to S
+ *              candidates (8 bytes each: every position of a row whose logits
+ *              rise with the position is a candidate), of which typically a
+ *              small part is written.  Calls that share it must not overlap.
+ * ------------------------------------------------------------------------ */
+IDX_API size_t idx_mqa_logits_topk_workspace_bytes(int64_t T, int64_t S, int32_t k);
+
+IDX_API idx_status idx_mqa_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales, int64_t T,
+                               int32_t H, const uint8_t* k_vals, const uint8_t* k_scales,
+                               int64_t S, const float* weights, const int32_t* row_start,
+                               const int32_t* row_end, int32_t k, int32_t* out_idx,
+                               void* workspace, size_t workspace_bytes,
+                               idx_device_errors* errors, idx_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * idx_topk_rows -- top-k per logits row (sparse_indexer docs: top_k_per_row
@@ -231,6 +306,39 @@ IDX_API idx_status idx_paged_logits_topk_noalloc(
     const uint8_t* kcache, int64_t num_blocks, int32_t page_size, const int32_t* block_table,
     int32_t max_blocks, const int32_t* context_lens, const float* weights, int32_t k,
     int32_t* out_idx, idx_device_errors* errors, idx_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * idx_paged_decode_step -- one decode step of the indexer in two launches:
+ * the step's insert (PR #48558, "Changes": indexer_k_quant_and_cache ahead of
+ * the paged reader) and query quantisation ("Notes") done by the scoring
+ * launch of idx_paged_logits_topk, before it scores, then its select.
+ *   k_new_bf16   [B*next_n, 128] bf16, contiguous, 16-byte aligned: the step's
+ *                new keys; row b*next_n + j is position L_b - next_n + j of
+ *                sequence b and is written to that position's page (through
+ *                the block table) and offset, as idx_quant_insert would.  A
+ *                position outside the block table, or a page id outside the
+ *                cache, is skipped and counted.
+ *   q_bf16       [B*next_n, H, 128] bf16, contiguous, 16-byte aligned: the
+ *                step's query heads, quantised as idx_quant_q would (into the
+ *                workspace; nothing else of the caller's is written).
+ *   The other arguments are those of idx_paged_logits_topk; context_lens
+ *   count the new tokens.  out_idx [B*next_n, k] as there.
+ *   workspace    at least idx_paged_decode_step_workspace_bytes(...) bytes,
+ *                256-byte aligned, no initialisation, not shared by calls that
+ *                overlap on the GPU.
+ *   The scoring launch is cooperative (every CTA resident at once, for the
+ *   grid-wide barrier between the insert and the reads).
+ * ------------------------------------------------------------------------ */
+IDX_API size_t idx_paged_decode_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H,
+                                             int32_t max_blocks, int32_t page_size, int32_t k);
+
+IDX_API idx_status idx_paged_decode_step(const void* k_new_bf16, const void* q_bf16, int32_t B,
+                                 int32_t next_n, int32_t H, uint8_t* kcache, int64_t num_blocks,
+                                 int32_t page_size, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* context_lens,
+                                 const float* weights, int32_t k, int32_t* out_idx,
+                                 void* workspace, size_t workspace_bytes,
+                                 idx_device_errors* errors, idx_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * idx_gather_k -- copy sequences' cached tokens into contiguous value/scale

@@ -45,6 +45,14 @@ SIGNATURES = {
                                     _P]),
     "idx_paged_logits_topk_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _I32, _P,
                                                      _I32, _P, _P, _I32, _P, _P, _P]),
+    "idx_paged_decode_step_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "idx_paged_decode_step": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _I32, _P, _I32,
+                                             _P, _P, _I32, _P, _P, _SZ, _P, _P]),
+    "idx_mqa_logits_topk_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
+    "idx_mqa_logits_topk": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _P, _I64, _P, _P, _P, _I32, _P,
+                                           _P, _SZ, _P, _P]),
+    "idx_rope_quant_q": (ctypes.c_int, [_P, _I64, _I32, _P, _P, _P, _I32, _I32, _P, _P, _P, _P]),
+    "idx_kpool_insert": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P]),
 }
 
 
@@ -148,6 +156,65 @@ def quant_q(q: torch.Tensor, out_vals=None, out_scales=None, stream=None):
     return vals, scales
 
 
+def rope_quant_q(q: torch.Tensor, positions: torch.Tensor, cos: torch.Tensor | None,
+                 sin: torch.Tensor | None, rot_dim: int, out_vals=None, out_scales=None,
+                 errors=None, stream=None):
+    """Rotary embedding of q ([T, H, 128] bf16) by table rows positions ([T]
+    int32) of cos/sin ([num_pos, rot_dim/2] fp32), fused with the MXFP4
+    quantisation: (vals [T*H, 64] uint8, scales [T*H, 4] uint8)."""
+    _need(q, torch.bfloat16, "q")
+    _need(positions, torch.int32, "positions")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be [T, H, 128]")
+    T, H = q.shape[0], q.shape[1]
+    if positions.numel() != T:
+        raise ValueError("positions must have one entry per token")
+    num_pos = 0
+    if rot_dim > 0:
+        _need(cos, torch.float32, "cos")
+        _need(sin, torch.float32, "sin")
+        if cos.shape != sin.shape or cos.dim() != 2 or cos.shape[1] != rot_dim // 2:
+            raise ValueError("cos/sin must be [num_pos, rot_dim / 2]")
+        num_pos = cos.shape[0]
+    rows = T * H
+    vals = out_vals if out_vals is not None else torch.empty((rows, 64), dtype=torch.uint8,
+                                                             device=q.device)
+    scales = out_scales if out_scales is not None else torch.empty((rows, 4), dtype=torch.uint8,
+                                                                   device=q.device)
+    _check("idx_rope_quant_q", lib.idx_rope_quant_q(
+        _ptr(q), T, H, _ptr(positions), _ptr(cos) if rot_dim > 0 else None,
+        _ptr(sin) if rot_dim > 0 else None, num_pos, rot_dim, _ptr(vals), _ptr(scales),
+        _ptr(errors), _stream(stream)))
+    return vals, scales
+
+
+def kpool_insert(k: torch.Tensor, gate: torch.Tensor, ape: torch.Tensor,
+                 slot_mapping: torch.Tensor, kcache: torch.Tensor, pooled=None, errors=None,
+                 stream=None) -> None:
+    """K-pool compressed insert: pools of kpool = ape.shape[0] keys of k
+    ([n, 128] bf16) weighted by a softmax of gate ([n, 128] fp32) plus ape
+    ([kpool, 128] fp32), written as MXFP4 keys at the pool-granular
+    slot_mapping ([n] int64) of kcache; pooled ([n, 128] fp32, optional)
+    receives the pooled vectors of the written rows."""
+    _need(k, torch.bfloat16, "k")
+    _need(gate, torch.float32, "gate")
+    _need(ape, torch.float32, "ape")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(kcache, torch.uint8, "kcache")
+    n = k.shape[0]
+    if k.dim() != 2 or k.shape[1] != HEAD_DIM or gate.shape != k.shape:
+        raise ValueError("k and gate must be [n, 128]")
+    if ape.dim() != 2 or ape.shape[1] != HEAD_DIM or slot_mapping.numel() != n:
+        raise ValueError("ape must be [kpool, 128] and slot_mapping [n]")
+    if pooled is not None:
+        _need(pooled, torch.float32, "pooled")
+        if pooled.shape != k.shape:
+            raise ValueError("pooled must be [n, 128]")
+    _check("idx_kpool_insert", lib.idx_kpool_insert(
+        _ptr(k), _ptr(gate), _ptr(ape), _ptr(slot_mapping), n, ape.shape[0], _ptr(kcache),
+        kcache.shape[0], PAGE_SIZE, _ptr(pooled), _ptr(errors), _stream(stream)))
+
+
 def _paged_common(q_vals, q_scales, weights, kcache, block_table, context_lens, next_n, H):
     _need(q_vals, torch.uint8, "q_vals")
     _need(q_scales, torch.uint8, "q_scales")
@@ -221,6 +288,42 @@ def paged_logits_topk_noalloc(q_vals, q_scales, weights, kcache, block_table, co
     return idx
 
 
+def paged_decode_step_workspace_bytes(B: int, next_n: int, H: int, max_blocks: int,
+                                      k: int) -> int:
+    return int(lib.idx_paged_decode_step_workspace_bytes(B, next_n, H, max_blocks, PAGE_SIZE, k))
+
+
+def paged_decode_step(k_new, q, weights, kcache, block_table, context_lens, next_n: int, H: int,
+                      k: int = 2048, workspace=None, out=None, errors=None, stream=None):
+    """One decode step: insert the step's new keys (k_new [B*next_n, 128] bf16,
+    at positions L_b - next_n + j through the block table), quantise its query
+    heads (q [B*next_n, H, 128] bf16) and return the top-k of every row
+    ([B*next_n, k] int32), in two launches."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(q, torch.bfloat16, "q")
+    _need(weights, torch.float32, "weights")
+    _need(kcache, torch.uint8, "kcache")
+    _need(block_table, torch.int32, "block_table")
+    _need(context_lens, torch.int32, "context_lens")
+    B = context_lens.numel()
+    max_blocks = block_table.shape[1]
+    if k_new.numel() != B * next_n * HEAD_DIM or q.numel() != B * next_n * H * HEAD_DIM:
+        raise ValueError("k_new / q do not match B * next_n (* H) rows of 128")
+    if weights.numel() != B * next_n * H:
+        raise ValueError("weights must be [B * next_n, H]")
+    if workspace is None:
+        n = paged_decode_step_workspace_bytes(B, next_n, H, max_blocks, k)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    _need(workspace, torch.uint8, "workspace")
+    idx = out if out is not None else torch.empty((B * next_n, k), dtype=torch.int32,
+                                                  device=q.device)
+    _check("idx_paged_decode_step", lib.idx_paged_decode_step(
+        _ptr(k_new), _ptr(q), B, next_n, H, _ptr(kcache), kcache.shape[0], PAGE_SIZE,
+        _ptr(block_table), max_blocks, _ptr(context_lens), _ptr(weights), k, _ptr(idx),
+        _ptr(workspace), workspace.numel(), _ptr(errors), _stream(stream)))
+    return idx
+
+
 def mqa_logits(q_vals, q_scales, weights, k_vals, k_scales, row_start, row_end, H: int,
                ld: int | None = None, clean: bool = False, out=None, errors=None, stream=None):
     _need(q_vals, torch.uint8, "q_vals")
@@ -241,6 +344,35 @@ def mqa_logits(q_vals, q_scales, weights, k_vals, k_scales, row_start, row_end, 
         _ptr(row_start), _ptr(row_end), _ptr(logits), ld, 1 if clean else 0, _ptr(errors),
         _stream(stream)))
     return logits
+
+
+def mqa_logits_topk_workspace_bytes(T: int, S: int, k: int) -> int:
+    return int(lib.idx_mqa_logits_topk_workspace_bytes(T, S, k))
+
+
+def mqa_logits_topk(q_vals, q_scales, weights, k_vals, k_scales, row_start, row_end, H: int,
+                    k: int = 2048, workspace=None, out=None, errors=None, stream=None):
+    """Prefill logits + top-k of every row without a logits tensor:
+    [T, k] int32 positions relative to row_start (-1 padded)."""
+    _need(q_vals, torch.uint8, "q_vals")
+    _need(q_scales, torch.uint8, "q_scales")
+    _need(k_vals, torch.uint8, "k_vals")
+    _need(k_scales, torch.uint8, "k_scales")
+    _need(weights, torch.float32, "weights")
+    _need(row_start, torch.int32, "row_start")
+    _need(row_end, torch.int32, "row_end")
+    T = row_end.numel()
+    S = k_vals.numel() // 64
+    if workspace is None:
+        workspace = torch.empty(max(mqa_logits_topk_workspace_bytes(T, S, k), 256),
+                                dtype=torch.uint8, device=q_vals.device)
+    _need(workspace, torch.uint8, "workspace")
+    idx = out if out is not None else torch.empty((T, k), dtype=torch.int32, device=q_vals.device)
+    _check("idx_mqa_logits_topk", lib.idx_mqa_logits_topk(
+        _ptr(q_vals), _ptr(q_scales), T, H, _ptr(k_vals), _ptr(k_scales), S, _ptr(weights),
+        _ptr(row_start), _ptr(row_end), k, _ptr(idx), _ptr(workspace), workspace.numel(),
+        _ptr(errors), _stream(stream)))
+    return idx
 
 
 def topk_rows(logits, row_end, k: int = 2048, row_start=None, out=None, stream=None):

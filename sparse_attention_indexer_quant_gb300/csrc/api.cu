@@ -106,6 +106,42 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The prefill kernels' 2-D tensor map over the contiguous key values: 64 bytes
+// x S rows, boxes of 128 rows, 64-byte swizzle (rows past S read as zeros).
+idx_status key_tensor_map(const uint8_t* k_vals, int64_t S, CUtensorMap* tk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {64, (cuuint64_t)S};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(k_vals), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (keys): CUresult %d", (int)r);
+  return IDX_OK;
+}
+
+// Workspace of the prefill logits + top-k: per row a list length, then
+// [rows][ld] candidate values and [rows][ld] positions (ld = S rounded up to 4).
+struct MqaTopkWs {
+  uint32_t* cnt;
+  float* vals;
+  int32_t* idx;
+  int64_t ld;
+};
+size_t ws_round(size_t x) { return (x + 255) / 256 * 256; }
+MqaTopkWs mqa_topk_ws(void* base, int64_t T, int64_t S, size_t* total) {
+  const int64_t ld = (S + 3) / 4 * 4;
+  const size_t o_cnt = 256, o_vals = o_cnt + ws_round((size_t)T * 4);
+  const size_t o_idx = o_vals + ws_round((size_t)T * ld * 4);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  MqaTopkWs w{reinterpret_cast<uint32_t*>(p + o_cnt), reinterpret_cast<float*>(p + o_vals),
+              reinterpret_cast<int32_t*>(p + o_idx), ld};
+  if (total) *total = o_idx + ws_round((size_t)T * ld * 4);
+  return w;
+}
+
 idx_status check_paged_common(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
                               int32_t next_n, int32_t H, const uint8_t* kcache,
                               int64_t num_blocks, int32_t page_size, const int32_t* block_table,
@@ -221,6 +257,51 @@ idx_status idx_quant_q(const void* q_bf16, int64_t rows, uint8_t* q_vals, uint8_
                    "quant_q launch");
 }
 
+idx_status idx_rope_quant_q(const void* q_bf16, int64_t T, int32_t H, const int32_t* positions,
+                            const float* cos_table, const float* sin_table, int32_t num_pos,
+                            int32_t rot_dim, uint8_t* q_vals, uint8_t* q_scales,
+                            idx_device_errors* errors, idx_stream_t stream) {
+  if (T < 0 || T > (int64_t)INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "T=%lld", (long long)T);
+  if (H <= 0 || H > 1024) return fail(IDX_ERR_INVALID_ARG, "H=%d outside [1, 1024]", H);
+  if (rot_dim < 0 || rot_dim > 128 || (rot_dim % 2) != 0)
+    return fail(IDX_ERR_INVALID_ARG, "rot_dim=%d (even, 0..128)", rot_dim);
+  if (num_pos < 0) return fail(IDX_ERR_INVALID_ARG, "num_pos=%d", num_pos);
+  idx_status s = idx::current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (T == 0) return ok();
+  if (!q_bf16 || !q_vals || !q_scales ||
+      (rot_dim > 0 && (!positions || !cos_table || !sin_table)))
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_bf16, 16) || !aligned(q_vals, 4) || !aligned(q_scales, 4) ||
+      !aligned(positions, 4) || !aligned(cos_table, 4) || !aligned(sin_table, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: q_bf16 16 bytes, the rest 4 bytes");
+  return from_cuda(idx::launch_rope_quant_q(q_bf16, T, H, positions, cos_table, sin_table,
+                                            num_pos, rot_dim, q_vals, q_scales, errors,
+                                            (cudaStream_t)stream),
+                   "rope_quant_q launch");
+}
+
+idx_status idx_kpool_insert(const void* k_bf16, const float* gate, const float* ape,
+                            const int64_t* slot_mapping, int64_t n, int32_t kpool,
+                            uint8_t* kcache, int64_t num_blocks, int32_t page_size,
+                            float* pooled, idx_device_errors* errors, idx_stream_t stream) {
+  if (n < 0 || n > (int64_t)INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "n=%lld", (long long)n);
+  if (kpool < 1 || kpool > 128) return fail(IDX_ERR_INVALID_ARG, "kpool=%d outside [1, 128]", kpool);
+  if (page_size != 64) return fail(IDX_ERR_INVALID_ARG, "page_size=%d (only 64)", page_size);
+  if (num_blocks <= 0) return fail(IDX_ERR_INVALID_ARG, "num_blocks=%lld", (long long)num_blocks);
+  idx_status s = idx::current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (n < kpool) return ok();  // no pool completes in this batch
+  if (!k_bf16 || !gate || !ape || !slot_mapping || !kcache)
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k_bf16, 16) || !aligned(kcache, 16) || !aligned(slot_mapping, 8) ||
+      !aligned(gate, 4) || !aligned(ape, 4) || !aligned(pooled, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: k_bf16/kcache 16 bytes, slots 8, floats 4");
+  return from_cuda(idx::launch_kpool_insert(k_bf16, gate, ape, slot_mapping, n, kpool, kcache,
+                                            num_blocks, pooled, errors, (cudaStream_t)stream),
+                   "kpool_insert launch");
+}
+
 idx_status idx_paged_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int32_t B,
                                 int32_t next_n, int32_t H, const uint8_t* kcache,
                                 int64_t num_blocks, int32_t page_size,
@@ -275,17 +356,8 @@ idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int64_
   if (!aligned(q_vals, 16) || !aligned(k_vals, 16) || !aligned(q_scales, 4) ||
       !aligned(k_scales, 4) || !aligned(weights, 4))
     return fail(IDX_ERR_INVALID_ARG, "alignment: q_vals/k_vals 16 bytes, scales/weights 4");
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   CUtensorMap tk;
-  const cuuint64_t dims[2] = {64, (cuuint64_t)S};
-  const cuuint64_t strides[1] = {64};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(k_vals), dims,
-                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "tensor map (keys): CUresult %d", (int)r);
+  if ((s = key_tensor_map(k_vals, S, &tk)) != IDX_OK) return s;
   idx::MqaArgs a{};
   a.q_vals = q_vals;
   a.q_scales = q_scales;
@@ -300,6 +372,66 @@ idx_status idx_mqa_logits(const uint8_t* q_vals, const uint8_t* q_scales, int64_
   a.clean = clean ? 1 : 0;
   a.errors = errors;
   return from_cuda(idx::launch_mqa_logits(tk, H, a, (cudaStream_t)stream), "mqa_logits launch");
+}
+
+size_t idx_mqa_logits_topk_workspace_bytes(int64_t T, int64_t S, int32_t k) {
+  (void)k;
+  if (T <= 0 || S <= 0) return 0;
+  size_t total = 0;
+  mqa_topk_ws(nullptr, T, S, &total);
+  return total;
+}
+
+idx_status idx_mqa_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales, int64_t T,
+                               int32_t H, const uint8_t* k_vals, const uint8_t* k_scales,
+                               int64_t S, const float* weights, const int32_t* row_start,
+                               const int32_t* row_end, int32_t k, int32_t* out_idx,
+                               void* workspace, size_t workspace_bytes,
+                               idx_device_errors* errors, idx_stream_t stream) {
+  if (T < 0 || T > (int64_t)INT32_MAX) return fail(IDX_ERR_INVALID_ARG, "T=%lld", (long long)T);
+  if (H != 32 && H != 64) return fail(IDX_ERR_INVALID_ARG, "H=%d not in {32,64}", H);
+  if (S < 0 || S > (int64_t)INT32_MAX - 256) return fail(IDX_ERR_INVALID_ARG, "S=%lld", (long long)S);
+  if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
+  idx_status s = idx::current_device_ok(nullptr);
+  if (s != IDX_OK) return s;
+  if (T == 0) return ok();
+  if (!out_idx || !row_start || !row_end) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (S == 0)  // every window is empty: every slot is -1
+    return from_cuda(cudaMemsetAsync(out_idx, 0xFF, (size_t)T * k * sizeof(int32_t),
+                                     (cudaStream_t)stream),
+                     "mqa_logits_topk (no keys)");
+  if (!q_vals || !q_scales || !k_vals || !k_scales || !weights)
+    return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_vals, 16) || !aligned(k_vals, 16) || !aligned(q_scales, 4) ||
+      !aligned(k_scales, 4) || !aligned(weights, 4))
+    return fail(IDX_ERR_INVALID_ARG, "alignment: q_vals/k_vals 16 bytes, scales/weights 4");
+  size_t need = 0;
+  const MqaTopkWs ws = mqa_topk_ws(workspace, T, S, &need);
+  if (workspace_bytes < need || workspace == nullptr)
+    return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  CUtensorMap tk;
+  if ((s = key_tensor_map(k_vals, S, &tk)) != IDX_OK) return s;
+  idx::MqaArgs a{};
+  a.q_vals = q_vals;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.weights = weights;
+  a.row_start = row_start;
+  a.row_end = row_end;
+  a.T = T;
+  a.S = S;
+  a.ld = S;
+  a.errors = errors;
+  a.topk = k;
+  a.cand_vals = ws.vals;
+  a.cand_idx = ws.idx;
+  a.cand_cnt = ws.cnt;
+  a.cand_ld = ws.ld;
+  cudaError_t e = idx::launch_mqa_logits(tk, H, a, (cudaStream_t)stream);
+  if (e == cudaSuccess)
+    e = idx::launch_cand_topk(ws.vals, ws.idx, ws.cnt, ws.ld, T, k, out_idx, (cudaStream_t)stream);
+  return from_cuda(e, "mqa_logits_topk launch");
 }
 
 idx_status idx_topk_rows(const float* logits, int64_t rows, int64_t ld, const int32_t* row_start,
@@ -377,6 +509,65 @@ idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q_scales,
   a.errors = errors;
   return from_cuda(idx::launch_paged_logits_topk(H, next_n, a, (cudaStream_t)stream),
                    "paged_logits_topk launch");
+}
+
+size_t idx_paged_decode_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H,
+                                             int32_t max_blocks, int32_t page_size, int32_t k) {
+  (void)page_size;
+  return idx::paged_step_workspace_bytes(B, next_n, H, max_blocks, k);
+}
+
+idx_status idx_paged_decode_step(const void* k_new_bf16, const void* q_bf16, int32_t B,
+                                 int32_t next_n, int32_t H, uint8_t* kcache, int64_t num_blocks,
+                                 int32_t page_size, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* context_lens,
+                                 const float* weights, int32_t k, int32_t* out_idx,
+                                 void* workspace, size_t workspace_bytes,
+                                 idx_device_errors* errors, idx_stream_t stream) {
+  // the checks of the fused call, on a placeholder for the quantised query
+  // (the step writes it into the workspace)
+  idx_status s = check_paged_common(reinterpret_cast<const uint8_t*>(q_bf16),
+                                    reinterpret_cast<const uint8_t*>(q_bf16), B, next_n, H, kcache,
+                                    num_blocks, page_size, block_table, max_blocks, context_lens,
+                                    weights);
+  if (s != IDX_OK) return s;
+  if (k < 1 || k > 2048) return fail(IDX_ERR_INVALID_ARG, "k=%d outside [1, 2048]", k);
+  int sms = 0;
+  if ((s = idx::current_device_ok(&sms)) != IDX_OK) return s;
+  if (B == 0) return ok();
+  if (!out_idx || !k_new_bf16) return fail(IDX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k_new_bf16, 16)) return fail(IDX_ERR_INVALID_ARG, "k_new not 16-byte aligned");
+  if ((int64_t)B * next_n > 65535)
+    return fail(IDX_ERR_INVALID_ARG, "B*next_n=%d above 65535", B * next_n);
+  const size_t need = idx::paged_step_workspace_bytes(B, next_n, H, max_blocks, k);
+  if (workspace_bytes < need || workspace == nullptr)
+    return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  idx::PagedArgs a{};
+  a.kcache = kcache;
+  a.kcache_w = kcache;
+  a.q_bf16 = static_cast<const uint16_t*>(q_bf16);
+  a.k_new = static_cast<const uint16_t*>(k_new_bf16);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.weights = weights;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.max_blocks = max_blocks;
+  const int32_t item_tiles = idx::paged_topk_item_tiles(
+      B, max_blocks, (int64_t)sms * idx::paged_ctas_per_sm(H * next_n));
+  set_paged_chunking(a, (int64_t)max_blocks * 64, sms, H * next_n, item_tiles);
+  if (a.chunks <= 0) return fail(IDX_ERR_INVALID_ARG, "max_blocks too large");
+  if ((int64_t)B * a.chunks + 2 * (int64_t)a.grid >= (int64_t(1) << idx::kItemBits) - 1)
+    return fail(IDX_ERR_INVALID_ARG, "B * work items per sequence = %lld too large",
+                (long long)B * a.chunks);
+  a.item_gen = next_item_generation();
+  a.topk = k;
+  a.out_idx = out_idx;
+  a.workspace = workspace;
+  a.errors = errors;
+  return from_cuda(idx::launch_paged_decode_step(H, next_n, a, (cudaStream_t)stream),
+                   "paged_decode_step launch");
 }
 
 idx_status idx_gather_k(const uint8_t* kcache, int64_t num_blocks, int32_t page_size,

@@ -24,6 +24,16 @@ cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_str
 cudaError_t launch_quant_q(const void* q, int64_t rows, uint8_t* vals, uint8_t* scales,
                            cudaStream_t stream);
 
+cudaError_t launch_rope_quant_q(const void* q, int64_t T, int32_t H, const int32_t* positions,
+                                const float* cs, const float* sn, int32_t num_pos,
+                                int32_t rot_dim, uint8_t* vals, uint8_t* scales,
+                                idx_device_errors* errors, cudaStream_t stream);
+
+cudaError_t launch_kpool_insert(const void* k, const float* gate, const float* ape,
+                                const int64_t* slots, int64_t n, int32_t kpool, uint8_t* cache,
+                                int64_t num_blocks, float* pooled, idx_device_errors* errors,
+                                cudaStream_t stream);
+
 // Paged decode (persistent kernels reading the cache with cp.async).
 struct PagedArgs {
   const uint8_t* kcache;
@@ -51,7 +61,37 @@ struct PagedArgs {
   int32_t wait_first;                // wait for the previous kernel before letting the
                                      // next one start (its early code may read the inputs)
   idx_device_errors* errors;
+  // decode step only (the scoring pass quantises the step's query heads and
+  // inserts its new keys before a grid-wide barrier)
+  const uint16_t* q_bf16;            // [rows, H, 128] bf16
+  const uint16_t* k_new;             // [rows, 128] bf16: row b*next_n + j at position
+                                     // L_b - next_n + j of sequence b
+  uint8_t* q_vals_w;                 // == q_vals, written by the prologue
+  uint8_t* q_scales_w;               // == q_scales
+  uint8_t* kcache_w;                 // == kcache
+  unsigned long long* grid_bar;      // generation-tagged arrival count
 };
+
+// Launches kern with programmatic stream serialization and as a cooperative
+// launch: every CTA of the grid is resident at once (the grid-wide barrier of
+// the decode step relies on it).
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 
@@ -97,6 +137,10 @@ cudaError_t launch_dependent_cluster(void (*kern)(KArgs...), dim3 grid, dim3 blo
 
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 size_t paged_topk_workspace_bytes(int32_t B, int32_t next_n, int32_t max_blocks, int32_t k);
+// the decode step: the fused call's workspace plus the quantised query heads
+size_t paged_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H, int32_t max_blocks,
+                                  int32_t k);
+cudaError_t launch_paged_decode_step(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 // 128-key tiles per work item of the fused scoring pass
 int32_t paged_topk_item_tiles(int32_t B, int32_t max_blocks, int64_t ctas);
 
@@ -115,9 +159,20 @@ struct MqaArgs {
   int64_t ld;
   int32_t clean;
   idx_device_errors* errors;
+  // logits + top-k: candidate lists instead of logits rows
+  int32_t topk;
+  float* cand_vals;       // [T][cand_ld] admitted logits
+  int32_t* cand_idx;      // [T][cand_ld] their positions in the row's window
+  uint32_t* cand_cnt;     // [T] list lengths
+  int64_t cand_ld;
 };
 cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs& a,
                               cudaStream_t stream);
+
+// top-k of every row's candidate list (the second launch of mqa_logits + top-k)
+cudaError_t launch_cand_topk(const float* cand_vals, const int32_t* cand_idx,
+                             const uint32_t* cand_cnt, int64_t cand_ld, int64_t rows, int32_t k,
+                             int32_t* out, cudaStream_t stream);
 
 cudaError_t launch_topk_rows(const float* logits, int64_t rows, int64_t ld,
                              const int32_t* row_start, const int32_t* row_end, int32_t k,

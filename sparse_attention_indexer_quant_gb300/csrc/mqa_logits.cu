@@ -18,6 +18,18 @@
 //               to each query's window.
 // The CTA order is reversed so that the largest groups (the end of a causal
 // prefill) start first.
+//
+// With TOPK (idx_mqa_logits_topk) no logits row is written: the epilogue keeps,
+// per query row, a histogram of the top 10 key bits (sign, exponent, one
+// mantissa bit) of the logits it has admitted and a threshold tau, the lower
+// edge of the histogram bin that holds the k-th largest admitted logit once k
+// are admitted.  A logit is admitted (appended to the row's candidate list,
+// value and position, with one shared-memory slot claim per warp) iff its key
+// is >= tau.  Every logit >= tau is therefore in the list and at least k of
+// them are, so the row's k largest are in the list; tau only grows (one warp
+// per query pair recomputes it every few tiles from a possibly stale, never
+// over-counted histogram).  A second kernel selects the exact top-k of each
+// list (topk.cu).
 #include <math.h>
 
 #include "common.cuh"
@@ -31,6 +43,18 @@ constexpr int kMqaThreads = 576;   // warp 0 TMA, warp 1 MMA, warps 2-17 epilogu
 constexpr int kMqaStages = 4;
 constexpr int kN = 256;            // query-head columns per CTA
 constexpr int kEpiWarps = 16;
+
+constexpr int kTkBins = 1024;      // candidate histogram: top 10 key bits
+constexpr int kTkShift = 22;
+constexpr int kTkEvery = 4;        // tiles between threshold updates
+
+// shared memory of the candidate state, per query of the group
+struct TopkState {
+  uint32_t hist[kTkBins];
+  uint32_t cnt;                    // candidates appended
+  uint32_t tau;                    // admission threshold (an order-preserving key)
+  uint32_t pad[2];
+};
 
 struct MqaLayout {
   static constexpr uint32_t kAccCol = 0;            // 256 fp32 columns
@@ -49,7 +73,40 @@ struct MqaLayout {
   static constexpr size_t kEnd = align_up(kMisc + 16, 1024);
 };
 
-template <int H>
+// The threshold of query q: the lower edge of the highest bin b with
+// count(bins >= b) >= k, or 0 while fewer than k are admitted.  One warp.
+__device__ __forceinline__ void update_tau(TopkState& ts, uint32_t k) {
+  const int lane = threadIdx.x & 31;
+  // lane l sums bins [kTkBins - 32 (l + 1), kTkBins - 32 l), the top ones first
+  const volatile uint32_t* h = ts.hist;
+  uint32_t c[32];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    c[i] = h[kTkBins - 1 - 32 * lane - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t run = incl - sum;
+  if (run < k && k <= incl) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (run < k && k <= run + c[i]) {
+        const uint32_t t = (uint32_t)(kTkBins - 1 - 32 * lane - i) << kTkShift;
+        if (t > ts.tau) ts.tau = t;
+      }
+      run += c[i];
+    }
+  }
+  __syncwarp();
+}
+
+template <int H, bool TOPK>
 __global__ void __launch_bounds__(kMqaThreads, 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_k, const MqaArgs p) {
   constexpr int G = kN / H;       // queries per CTA
@@ -90,6 +147,11 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
     }
     sStart[threadIdx.x] = st;
     sEnd[threadIdx.x] = en;
+  }
+  TopkState* tks = reinterpret_cast<TopkState*>(sm + Lay::kEnd);  // TOPK only
+  if (TOPK) {
+    for (int i = threadIdx.x; i < G * (int)(sizeof(TopkState) / 4); i += kMqaThreads)
+      reinterpret_cast<uint32_t*>(tks)[i] = 0u;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
@@ -251,11 +313,36 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
       for (int j = 0; j < GH; ++j) {
         const int64_t t = t0 + half * GH + j;
         if (t >= p.T) break;
-        float* row = p.logits + t * p.ld;
-        if (key >= st[j] && key < en[j])
-          row[key] = logit[j];
-        else if (p.clean && key < p.S)
-          row[key] = -INFINITY;
+        if (TOPK) {
+          // admit the logit if it reaches the row's threshold: one slot claim
+          // per warp (the warp's 32 keys belong to the same query)
+          TopkState& ts = tks[half * GH + j];
+          const uint32_t kk = float_key(logit[j]);
+          const bool take = key >= st[j] && key < en[j] && kk >= *(volatile uint32_t*)&ts.tau;
+          const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+          if (ballot != 0u) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&ts.cnt, (uint32_t)__popc(ballot));
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            if (take) {
+              const int64_t slot = t * p.cand_ld + base + __popc(ballot & ((1u << lane) - 1u));
+              p.cand_vals[slot] = logit[j];
+              p.cand_idx[slot] = (int32_t)(key - st[j]);
+              atomicAdd(&ts.hist[kk >> kTkShift], 1u);
+            }
+          }
+        } else {
+          float* row = p.logits + t * p.ld;
+          if (key >= st[j] && key < en[j])
+            row[key] = logit[j];
+          else if (p.clean && key < p.S)
+            row[key] = -INFINITY;
+        }
+      }
+      // one warp per query pair (its lane quarter 0) raises the thresholds
+      if (TOPK && quarter == 0 && (i % kTkEvery) == kTkEvery - 1) {
+#pragma unroll
+        for (int j = 0; j < GH; ++j) update_tau(tks[half * GH + j], (uint32_t)p.topk);
       }
     }
   }
@@ -265,6 +352,10 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+  if (TOPK) {
+    if (threadIdx.x < G && t0 + threadIdx.x < p.T) p.cand_cnt[t0 + threadIdx.x] = tks[threadIdx.x].cnt;
+    return;
   }
   if (p.clean) {
     // -inf for the columns of [0, S) that no tile covers
@@ -282,10 +373,10 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
   }
 }
 
-template <int H>
+template <int H, bool TOPK>
 cudaError_t launch_h(const CUtensorMap& tm, const MqaArgs& a, cudaStream_t stream) {
-  const size_t smem = MqaLayout::kEnd + 1024;
-  auto kern = mqa_logits_kernel<H>;
+  const size_t smem = MqaLayout::kEnd + (TOPK ? (kN / H) * sizeof(TopkState) : 0) + 1024;
+  auto kern = mqa_logits_kernel<H, TOPK>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -300,8 +391,9 @@ cudaError_t launch_h(const CUtensorMap& tm, const MqaArgs& a, cudaStream_t strea
 cudaError_t launch_mqa_logits(const CUtensorMap& tm_kvals, int H, const MqaArgs& a,
                               cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  if (H == 32) return launch_h<32>(tm_kvals, a, stream);
-  if (H == 64) return launch_h<64>(tm_kvals, a, stream);
+  const bool topk = a.cand_vals != nullptr;
+  if (H == 32) return topk ? launch_h<32, true>(tm_kvals, a, stream) : launch_h<32, false>(tm_kvals, a, stream);
+  if (H == 64) return topk ? launch_h<64, true>(tm_kvals, a, stream) : launch_h<64, false>(tm_kvals, a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "mxfp4_encode.cuh"
 
 namespace idx {
 
@@ -175,12 +176,88 @@ __device__ __forceinline__ void install_generation(unsigned long long* ctr, unsi
   }
 }
 
+// The decode step's prologue (a scoring pass that also does the step's
+// insert and query quantisation), run by every thread of every CTA before the
+// streaming loop: the grid's 16-thread groups take, in turn, the step's query
+// heads (rows * H vectors, quantised into q_vals_w / q_scales_w) and then its
+// new keys (row b * NEXT_N + j to position L_b - NEXT_N + j of sequence b,
+// through the block table, quantised into the cache), and the grid then meets
+// at a barrier: a generation-tagged arrival count in the workspace (the launch
+// is cooperative, so every CTA is resident), waited on by one thread per CTA
+// for at most kWaitLimitNs.  A new key whose position is outside the block
+// table or whose page id is outside the cache is skipped and counted.
+// Returns false (and raises *abort) if the barrier gave up.
+template <int H, int NEXT_N>
+__device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatile int* abort) {
+  const int64_t rows = (int64_t)p.B * NEXT_N;
+  const int64_t n_q = rows * H;
+  const int64_t n_vec = n_q + rows;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int part = lane & 15;
+  const int64_t cap = (int64_t)p.max_blocks * kPage;
+  const int64_t stride = (int64_t)gridDim.x * (kPagedThreads / 16);
+  // whole warps stay converged through the encoder's shuffles: a group past
+  // the end encodes zeros and stores nothing
+  for (int64_t base = ((int64_t)blockIdx.x * (kPagedThreads / 32) + warp) * 2; base < n_vec;
+       base += stride) {
+    const int64_t v = base + (lane >> 4);
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    uint8_t* vdst = nullptr;
+    uint8_t* sdst = nullptr;
+    if (v < n_q) {
+      raw = __ldg(reinterpret_cast<const uint4*>(p.q_bf16 + v * kHeadDim) + part);
+      vdst = p.q_vals_w + v * kValBytes;
+      sdst = p.q_scales_w + v * kScaleBytes;
+    } else if (v < n_vec) {
+      const int64_t r = v - n_q;
+      const int64_t b = r / NEXT_N, j = r % NEXT_N;
+      int64_t L = __ldg(p.context_lens + b);
+      L = L < 0 ? 0 : (L > cap ? cap : L);  // (an over-long context is counted by the loop)
+      const int64_t pos = L - NEXT_N + j;
+      const int32_t id = pos >= 0 ? __ldg(p.block_table + b * p.max_blocks + pos / kPage) : -1;
+      if (pos >= 0 && id >= 0 && id < p.num_blocks) {
+        raw = __ldg(reinterpret_cast<const uint4*>(p.k_new + r * kHeadDim) + part);
+        uint8_t* pg = p.kcache_w + (int64_t)id * kPageBytes;
+        vdst = pg + (pos % kPage) * kValBytes;
+        sdst = pg + kPageValBytes + (pos % kPage) * kScaleBytes;
+      } else if (part == 0) {
+        count_bad_input(p.errors);
+      }
+    }
+    uint32_t sw;
+    const uint32_t packed = encode8(raw, &sw);
+    if (vdst != nullptr) {
+      reinterpret_cast<uint32_t*>(vdst)[part] = packed;
+      if (part == 0) *reinterpret_cast<uint32_t*>(sdst) = sw;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    constexpr unsigned long long kCount = (1ull << kItemBits) - 1ull;
+    __threadfence();  // the CTA's writes before its arrival
+    claim_item(p.grid_bar, p.item_gen, p.errors);
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+      unsigned long long c;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(p.grid_bar) : "memory");
+      if ((c >> kItemBits) == p.item_gen && (c & kCount) >= gridDim.x) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        flag_timeout(p.errors, kTimeoutProducer);
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  return *abort == 0;
+}
+
 // Barrier among the four epilogue warps only.
 __device__ __forceinline__ void epilogue_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
-template <int H, int NEXT_N, class Ep>
+template <int H, int NEXT_N, class Ep, bool STEP = false>
 __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const uint8_t* kcache,
                                                      bool dynamic, bool pass_empty,
                                                      unsigned long long* item_counter) {
@@ -244,6 +321,8 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     pdl_launch_dependents();
     pdl_wait();
   }
+  // the decode step's insert and query quantisation, then the grid barrier
+  if (STEP) decode_step_prologue<H, NEXT_N>(p, abort);
   // The item loader's operands (warp 5), read into registers before they are
   // staged, all loads of a lane in flight together:
   //   B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
@@ -259,11 +338,14 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   int32_t id_r[4];
   auto load_operands = [&](int32_t b, int64_t k0, int32_t n_tiles) {
     const uint4* qv = reinterpret_cast<const uint4*>(p.q_vals + (int64_t)b * NH * kValBytes);
+    // (in the decode step this kernel's prologue wrote them: loads through L2)
 #pragma unroll
-    for (int u = 0; u < kQv; ++u) qv_r[u] = __ldg(qv + lane + 32 * u);
+    for (int u = 0; u < kQv; ++u) qv_r[u] = STEP ? __ldcg(qv + lane + 32 * u) : __ldg(qv + lane + 32 * u);
     const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)b * NH;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) sf_r[u] = lane + 32 * u < NH ? __ldg(qs + lane + 32 * u) : 0u;
+    for (int u = 0; u < 4; ++u)
+      sf_r[u] = lane + 32 * u < NH ? (STEP ? __ldcg(qs + lane + 32 * u) : __ldg(qs + lane + 32 * u))
+                                   : 0u;
 #pragma unroll
     for (int u = 0; u < NH / 32; ++u) w_r[u] = __ldg(p.weights + (int64_t)b * NH + lane + 32 * u);
     const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks + k0 / kPage;

@@ -10,6 +10,8 @@
 // to the logits row (-inf past the window when the rows are clean).
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "paged_core.cuh"
@@ -55,35 +57,74 @@ struct UnfusedEpilogue {
   }
 };
 
-template <int H, int NEXT_N>
+// STEP: the decode step's scoring pass, which first inserts the step's new
+// keys and quantises its query heads (decode_step_prologue), launched as a
+// cooperative grid.
+template <int H, int NEXT_N, bool STEP>
 __global__ void __launch_bounds__(kPagedThreads, paged_ctas_per_sm(H * NEXT_N))
     paged_logits_kernel(const PagedArgs p) {
-  paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>>(
+  paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>, STEP>(
       p, p.kcache, p.item_counter != nullptr, p.clean != 0, p.item_counter);
 }
 
-template <int H, int NEXT_N>
+// CTAs of the kernel resident per SM by the occupancy calculator, once per
+// device: the cooperative launch of the decode step is refused beyond it.
+template <int H, int NEXT_N, bool STEP>
+int resident_ctas_per_sm(size_t smem, int planned) {
+  auto kern = paged_logits_kernel<H, NEXT_N, STEP>;  // one cache per kernel
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return planned;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kPagedThreads, smem) !=
+            cudaSuccess ||
+        n <= 0) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    cache[dev] = n < planned ? n : planned;
+  }
+  return cache[dev];
+}
+
+template <int H, int NEXT_N, bool STEP>
 cudaError_t launch_one(const PagedArgs& a, cudaStream_t stream) {
   using Ep = UnfusedEpilogue<H, NEXT_N>;
   const size_t smem = paged_smem_bytes<H * NEXT_N>() + Ep::kExtraSmem;
-  auto kern = paged_logits_kernel<H, NEXT_N>;
+  auto kern = paged_logits_kernel<H, NEXT_N, STEP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3((unsigned)a.grid), dim3(kPagedThreads), smem, stream, a);
+  if (!STEP)
+    return launch_dependent(kern, dim3((unsigned)a.grid), dim3(kPagedThreads), smem, stream, a);
+  // the cooperative launch: no more CTAs than the runtime counts as resident
+  const int per_sm = resident_ctas_per_sm<H, NEXT_N, STEP>(smem, paged_ctas_per_sm(H * NEXT_N));
+  const int64_t cap = (int64_t)(a.sms > 0 ? a.sms : 1) * per_sm;
+  const unsigned grid = (unsigned)(a.grid < cap ? a.grid : cap);
+  return launch_dependent_coop(kern, dim3(grid), dim3(kPagedThreads), smem, stream, a);
+}
+
+template <bool STEP>
+cudaError_t launch_shape(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
+  if (H == 32 && next_n == 1) return launch_one<32, 1, STEP>(a, stream);
+  if (H == 32 && next_n == 2) return launch_one<32, 2, STEP>(a, stream);
+  if (H == 64 && next_n == 1) return launch_one<64, 1, STEP>(a, stream);
+  if (H == 64 && next_n == 2) return launch_one<64, 2, STEP>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
-  if (H == 32 && next_n == 1) return launch_one<32, 1>(a, stream);
-  if (H == 32 && next_n == 2) return launch_one<32, 2>(a, stream);
-  if (H == 64 && next_n == 1) return launch_one<64, 1>(a, stream);
-  if (H == 64 && next_n == 2) return launch_one<64, 2>(a, stream);
-  return cudaErrorInvalidValue;
+  return a.grid_bar != nullptr ? launch_shape<true>(H, next_n, a, stream)
+                               : launch_shape<false>(H, next_n, a, stream);
 }
 
 }  // namespace idx

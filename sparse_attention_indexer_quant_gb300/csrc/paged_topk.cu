@@ -28,22 +28,32 @@ namespace {
 
 struct TopkWs {
   unsigned long long* items;  // work-item counter of the scoring pass
+  unsigned long long* bar;    // the decode step's grid-barrier arrivals
   float* logits;              // [rows][ldw]
   int64_t ldw;
+  uint8_t* q_vals;            // decode step: quantised query heads [rows * H][64]
+  uint8_t* q_scales;          //              and their scales [rows * H][4]
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
 
+// H = 0: the fused call's workspace; H > 0: the decode step's, which also
+// holds the step's quantised query heads after the logits.
 __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t max_blocks,
-                                            size_t* total) {
+                                            size_t* total, int32_t H = 0) {
   const int64_t ldw = (int64_t)max_blocks * kPage;
   const size_t o_lg = 256;
+  const size_t o_qv = o_lg + ws_align((size_t)rows * ldw * 4);
+  const size_t o_qs = o_qv + ws_align((size_t)rows * H * kValBytes);
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
   w.items = reinterpret_cast<unsigned long long*>(p);
+  w.bar = w.items + 1;
   w.logits = reinterpret_cast<float*>(p + o_lg);
   w.ldw = ldw;
-  if (total) *total = o_lg + ws_align((size_t)rows * ldw * 4);
+  w.q_vals = H > 0 ? p + o_qv : nullptr;
+  w.q_scales = H > 0 ? p + o_qs : nullptr;
+  if (total) *total = H > 0 ? o_qs + ws_align((size_t)rows * H * kScaleBytes) : o_qv;
   return w;
 }
 
@@ -61,9 +71,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   // before the call completed
   int64_t L = __ldg(p.context_lens + b);
   pdl_wait();  // the scoring pass's logits
-  // the work-item counter is done with: clear it, so that a replay of this
-  // call with the same generation (a CUDA graph) finds no claims of its own
-  if (blockIdx.x == 0 && threadIdx.x == 0) *ws.items = 0ull;
+  // the work-item counter (and the decode step's barrier count) are done
+  // with: clear them, so that a replay of this call with the same generation
+  // (a CUDA graph) finds no claims or arrivals of its own
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    ws.items[0] = 0ull;
+    ws.items[1] = 0ull;
+  }
   const int64_t cap = (int64_t)p.max_blocks * kPage;
   L = L < 0 ? 0 : (L > cap ? cap : L);
   int64_t len = L - next_n + j + 1;
@@ -90,6 +104,27 @@ int32_t paged_topk_item_tiles(int32_t B, int32_t max_blocks, int64_t ctas) {
   const int64_t tiles = (int64_t)B * (((int64_t)max_blocks * kPage + kTileKeys - 1) / kTileKeys);
   const int64_t per = tiles / ((ctas > 0 ? ctas : 1) * 8);
   return per < 6 ? 4 : (per < 12 ? 8 : 16);
+}
+
+size_t paged_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H, int32_t max_blocks,
+                                  int32_t k) {
+  (void)k;
+  if (B <= 0 || (next_n != 1 && next_n != 2) || max_blocks <= 0 || H <= 0) return 0;
+  size_t total = 0;
+  ws_layout(nullptr, (int64_t)B * next_n, max_blocks, &total, H);
+  return total;
+}
+
+cudaError_t launch_paged_decode_step(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
+  const int64_t rows = (int64_t)a.B * next_n;
+  const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr, H);
+  PagedArgs s = a;
+  s.q_vals = ws.q_vals;
+  s.q_scales = ws.q_scales;
+  s.q_vals_w = ws.q_vals;
+  s.q_scales_w = ws.q_scales;
+  s.grid_bar = ws.bar;
+  return launch_paged_logits_topk(H, next_n, s, stream);
 }
 
 cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {

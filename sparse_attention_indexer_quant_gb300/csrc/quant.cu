@@ -13,6 +13,7 @@
 // reading their inputs.
 #include "common.cuh"
 #include "launch.h"
+#include "mxfp4_encode.cuh"
 
 namespace idx {
 
@@ -21,55 +22,6 @@ namespace {
 constexpr int kThreadsPerVec = 16;
 constexpr int kBlockThreads = 256;
 constexpr int kVecsPerBlock = kBlockThreads / kThreadsPerVec;
-
-// Quantise the 8 values held by this thread (as 4 x bf16x2 words) of a vector
-// whose 16 owner threads are lanes [16*g, 16*g + 16) of the warp.  Returns the
-// 4 packed value bytes; *scales_word gets the vector's 4 scale bytes (valid in
-// every lane).
-__device__ __forceinline__ uint32_t encode8(uint4 raw, uint32_t* scales_word) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t amax = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    amax = max(amax, w[i] & 0x7FFFu);
-    amax = max(amax, (w[i] >> 16) & 0x7FFFu);
-  }
-  // four consecutive lanes hold one block of 32
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  const uint32_t s = ue8m0_of_amax(amax << 16);
-  const float inv = inv_scale_of(s);
-  // x * 2^-e is exact for every magnitude that can round to a nonzero code;
-  // the hardware convert rounds to nearest with ties to the even code,
-  // saturates at 6 and keeps the sign of a value that rounds to zero (the
-  // rule of the exhaustive bf16 test); element 2i goes to the low nibble of
-  // byte i
-  float y[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    y[2 * i] = __uint_as_float(w[i] << 16) * inv;
-    y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u) * inv;
-  }
-  uint32_t packed;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(packed)
-      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
-  // gather the 4 block scales of this vector: blocks live in lanes 0,4,8,12 of
-  // the 16-lane group
-  const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t base = lane & 16u;
-  const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, s, base + 0);
-  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, s, base + 4);
-  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, s, base + 8);
-  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, s, base + 12);
-  *scales_word = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
-  return packed;
-}
 
 // Each 16-thread group quantises VPG vectors (rows u * gstride + vec for
 // u < VPG): all of a thread's loads are issued before any encode, so each
@@ -147,7 +99,71 @@ __global__ void __launch_bounds__(kBlockThreads) quant_q_kernel(const uint16_t* 
   }
 }
 
+// Rotary embedding of the query heads fused with their quantisation (vLLM PR
+// #48558 "Notes": a fused q-rope + MXFP4 q-quant): the thread owning elements
+// [8*part, 8*part + 8) turns its pairs (2i, 2i+1) with i < rot_dim / 2 by the
+// angle of table column i at the token's position, in fp32 with the products
+// y*sin and y*cos rounded first and then one fused multiply-add each, and the
+// 16 threads of the vector encode the result.  A token whose position is
+// outside the table is skipped (its rows are not written) and counted.
+__global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
+    const uint16_t* __restrict__ q, int64_t T, int32_t H, const int32_t* __restrict__ positions,
+    const float* __restrict__ cs, const float* __restrict__ sn, int32_t num_pos, int32_t rot_dim,
+    uint8_t* __restrict__ vals, uint8_t* __restrict__ scales, idx_device_errors* errors) {
+  const int64_t vec = (int64_t)blockIdx.x * kVecsPerBlock + threadIdx.x / kThreadsPerVec;
+  const int part = threadIdx.x % kThreadsPerVec;
+  const int64_t rows = T * H;
+  const int half = rot_dim / 2;
+  pdl_launch_dependents();
+  pdl_wait();  // inputs may come from the previous kernel
+  // whole warps stay converged through the shuffles: rows past the end and
+  // tokens off the table run the arithmetic on zeros and skip the stores
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  int32_t pos = 0;
+  bool live = vec < rows;
+  if (live) {
+    raw = __ldg(reinterpret_cast<const uint4*>(q + vec * kHeadDim) + part);
+    pos = half > 0 ? __ldg(positions + vec / H) : 0;  // no table without rotated pairs
+    if (half > 0 && (pos < 0 || pos >= num_pos)) {
+      if (part == 0 && vec % H == 0) count_bad_input(errors);
+      live = false;
+      pos = 0;
+    }
+  }
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  const float* c_row = cs + (int64_t)pos * half;
+  const float* s_row = sn + (int64_t)pos * half;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int col = 4 * part + i;  // pair (8 * part + 2i, 8 * part + 2i + 1)
+    if (live && col < half) {
+      const float c = __ldg(c_row + col), s = __ldg(s_row + col);
+      const float a = x[2 * i], b = x[2 * i + 1];
+      x[2 * i] = __fmaf_rn(a, c, -__fmul_rn(b, s));
+      x[2 * i + 1] = __fmaf_rn(a, s, __fmul_rn(b, c));
+    }
+  }
+  uint32_t sw;
+  const uint32_t packed = encode8_f32(x, &sw);
+  if (!live) return;
+  reinterpret_cast<uint32_t*>(vals + vec * kValBytes)[part] = packed;
+  if (part == 0) reinterpret_cast<uint32_t*>(scales)[vec] = sw;
+}
+
 }  // namespace
+
+cudaError_t launch_rope_quant_q(const void* q, int64_t T, int32_t H, const int32_t* positions,
+                                const float* cs, const float* sn, int32_t num_pos,
+                                int32_t rot_dim, uint8_t* vals, uint8_t* scales,
+                                idx_device_errors* errors, cudaStream_t stream) {
+  const int64_t rows = T * H;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + kVecsPerBlock - 1) / kVecsPerBlock;
+  return launch_dependent(rope_quant_q_kernel, dim3((unsigned)blocks), dim3(kBlockThreads), 0,
+                          stream, static_cast<const uint16_t*>(q), T, H, positions, cs, sn,
+                          num_pos, rot_dim, vals, scales, errors);
+}
 
 cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_stride,
                                 const int64_t* slots, uint8_t* cache, int64_t num_blocks,

@@ -47,7 +47,39 @@ __global__ void __launch_bounds__(kRowThreads, 4) topk_rows_kernel(const float* 
   row_topk(sm, logits + row * ld + st, en > st ? en - st : 0, k, out + row * k);
 }
 
+// Top-k of a candidate list (prefill logits + top-k): row_topk over the list's
+// values gives list positions, which are then replaced by the positions in
+// the row's window that the list stores beside each value.
+__global__ void __launch_bounds__(kRowThreads, 4) cand_topk_kernel(
+    const float* __restrict__ cand_vals, const int32_t* __restrict__ cand_idx,
+    const uint32_t* __restrict__ cand_cnt, int64_t cand_ld, int32_t k, int32_t* out) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  RowsSmem& sm = *reinterpret_cast<RowsSmem*>(smem_raw);
+  pdl_wait();  // the lists come from the previous kernel
+  const int64_t row = blockIdx.x;
+  const int64_t n = __ldg(cand_cnt + row);
+  int32_t* o = out + row * k;
+  row_topk(sm, cand_vals + row * cand_ld, n, k, o);
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += kRowThreads) {
+    const int32_t pos = o[i];
+    if (pos >= 0) o[i] = __ldg(cand_idx + row * cand_ld + pos);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_cand_topk(const float* cand_vals, const int32_t* cand_idx,
+                             const uint32_t* cand_cnt, int64_t cand_ld, int64_t rows, int32_t k,
+                             int32_t* out, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = sizeof(RowsSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(cand_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(cand_topk_kernel, dim3((unsigned)rows), dim3(kRowThreads), smem, stream,
+                          cand_vals, cand_idx, cand_cnt, cand_ld, k, out);
+}
 
 cudaError_t launch_topk_rows(const float* logits, int64_t rows, int64_t ld,
                              const int32_t* row_start, const int32_t* row_end, int32_t k,

@@ -365,6 +365,8 @@ def run_ours(args, rank, world, local_rank):
         also = secondary_measurements(idx, dev, flush_l2, stream,
                                       decode=(p, cache, qv, qs, w, bt, cl))
         also.update(insert_entries(idx, dev, flush_l2, stream))
+        also.update(next_entries(idx, dev, flush_l2, stream))
+        also.update(step_entries(idx, dev, flush_l2, stream))
         for other in ("long_decode", "mixed_decode", "pr_ref"):
             if other != args.workload:
                 also[other] = decode_workload_entry(other, idx, dev, flush_l2, stream)
@@ -570,6 +572,94 @@ def prefill_oracle_sample(p, qv, qs, kv, ks, logits_dev, n_rows=512, seed=4242):
             "gpu_logits_match_oracle_on_sample": ok}
 
 
+def step_entries(idx, dev, flush_l2, stream, reps=50):
+    """The two-launch decode step (insert and q-quant inside the scoring
+    launch) against the four separate calls, each step captured as a CUDA
+    graph and replayed with L2 flushed before each: on the 8K
+    single-sequence decode and on the 64-sequence batched decode."""
+    import torch
+    res = {}
+    for name in ("pr_ref", "batched_decode"):
+        p = make_workload(name)
+        new = p.new_token_rows()
+        old = np.setdiff1d(np.arange(p.total_tokens), new)
+        cache = fill_cache(idx, p, dev, rows=old)
+        new_k = bf16_tensor(p.k[new], dev)
+        new_slots = torch.from_numpy(p.slots[new]).to(dev)
+        q = bf16_tensor(p.q, dev)
+        w = torch.from_numpy(p.weights).to(dev)
+        bt = torch.from_numpy(p.block_table).to(dev)
+        cl = torch.from_numpy(p.context_lens).to(dev)
+        mb = p.block_table.shape[1]
+        ws = idx.new_paged_topk_workspace(p.B, p.next_n, mb, TOPK, dev)
+        ws_step = torch.empty(idx.paged_decode_step_workspace_bytes(p.B, p.next_n, p.H, mb, TOPK),
+                              dtype=torch.uint8, device=dev)
+        qv = torch.empty((p.rows * p.H, 64), dtype=torch.uint8, device=dev)
+        qs = torch.empty((p.rows * p.H, 4), dtype=torch.uint8, device=dev)
+        out = torch.empty((p.rows, TOPK), dtype=torch.int32, device=dev)
+
+        def four():
+            idx.quant_insert(new_k, new_slots, cache)
+            idx.quant_q(q, out_vals=qv, out_scales=qs)
+            idx.paged_logits_topk(qv, qs, w, cache, bt, cl, p.next_n, p.H, TOPK, workspace=ws,
+                                  out=out)
+
+        def two():
+            idx.paged_decode_step(new_k, q, w, cache, bt, cl, p.next_n, p.H, TOPK,
+                                  workspace=ws_step, out=out)
+
+        ms4 = time_op(graph_of(four).replay, flush_l2, stream, reps)
+        ms2 = time_op(graph_of(two).replay, flush_l2, stream, reps)
+        res[f"decode_step_{name}"] = {
+            "workload": WORKLOADS[name][1],
+            "two_launch_step_us": ms2 * 1e3, "four_launch_step_us": ms4 * 1e3,
+            "timing": f"median of {reps} CUDA-graph replays, L2 flushed before each",
+            "note": "the two-launch step's scoring launch is cooperative, so the runtime caps it "
+                    "at one CTA per SM"}
+        del cache
+    return res
+
+
+def next_entries(idx, dev, flush_l2, stream, reps=10):
+    """The fused q-RoPE + q-quant on the causal prefill's query heads and the
+    K-pool insert of its keys (pool 4, seeded gates)."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    hbm, _ = peaks()
+    p = wl.prefill()
+    q = bf16_tensor(p.q, dev)
+    g = wl.rng(4711)
+    half = 32
+    ang = np.arange(p.T, dtype=np.float64)[:, None] * 10000.0 ** (-np.arange(half) / half)[None, :]
+    cs = torch.from_numpy(np.cos(ang).astype(np.float32)).to(dev)
+    sn = torch.from_numpy(np.sin(ang).astype(np.float32)).to(dev)
+    pos = torch.arange(p.T, dtype=torch.int32, device=dev)
+    qv, qs = idx.rope_quant_q(q, pos, cs, sn, 64)
+    ms = time_op(lambda: idx.rope_quant_q(q, pos, cs, sn, 64, out_vals=qv, out_scales=qs),
+                 flush_l2, stream, reps)
+    rows = p.T * p.H
+    b = rows * (256 + 68) + p.T * (4 + 2 * half * 4)
+    res = {"rope_quant_q": {"workload": f"{rows} query-head rows of the causal prefill, rot_dim 64",
+                            "ms": ms, "gbs": b / (ms * 1e-3) / 1e9,
+                            "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm}}
+    P = 4
+    n = p.T
+    k = bf16_tensor(p.k, dev)
+    gate = torch.from_numpy(g.standard_normal((n, 128)).astype(np.float32)).to(dev)
+    ape = torch.from_numpy(g.standard_normal((P, 128)).astype(np.float32)).to(dev)
+    slots = np.full(n, -1, np.int64)
+    slots[P - 1::P] = np.arange(n // P)
+    num_blocks = (n // P + 63) // 64
+    cache = torch.from_numpy(wl.poisoned_cache(num_blocks)).to(dev)
+    sl = torch.from_numpy(slots).to(dev)
+    ms = time_op(lambda: idx.kpool_insert(k, gate, ape, sl, cache), flush_l2, stream, reps)
+    b = n * (256 + 512 + 8) + P * 512 + (n // P) * 68
+    res["kpool_insert"] = {"workload": f"{n} keys of the causal prefill in pools of {P}",
+                           "ms": ms, "gbs": b / (ms * 1e-3) / 1e9,
+                           "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm}
+    return res
+
+
 def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
     """The other steps of the path, each timed alone with a flushed L2: insert,
     q-quant, gather, prefill logits and top-k on the 32K-token causal prefill
@@ -631,6 +721,13 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
                       flush_l2, stream, reps)
     pre_cpu = prefill_oracle_sample(p, qv, qs, kv, ks, logits)
     del logits
+    # the same rows' top-k without a logits tensor (candidate lists)
+    ws_tk = torch.empty(idx.mqa_logits_topk_workspace_bytes(p.T, S, TOPK), dtype=torch.uint8,
+                        device=dev)
+    fused_ms = time_op(lambda: idx.mqa_logits_topk(qv, qs, w, kv, ks, st_d, en_d, p.H, TOPK,
+                                                   workspace=ws_tk, out=out),
+                       flush_l2, stream, reps)
+    del ws_tk
     tf = flops / (pre_ms * 1e-3) / 1e12
     res.update({
         "q_quant": {"workload": f"{q_rows} query-head rows of the causal prefill", "ms": qq_ms,
@@ -651,6 +748,10 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
         "prefill_topk": {"workload": "32768 causal rows, k=2048", "ms": topk_ms,
                          "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9},
         "prefill_cpu_baseline": pre_cpu,
+        "prefill_logits_topk_fused": {
+            "workload": "causal 32768 x 32768, H=32, k=2048, no logits tensor",
+            "ms": fused_ms, "unfused_ms": pre_ms + topk_ms,
+            "tflops": tf * pre_ms / fused_ms},
     })
     return res
 

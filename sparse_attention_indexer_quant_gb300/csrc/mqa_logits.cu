@@ -7,12 +7,14 @@
 // One CTA per group of G = 256 / H query tokens: the group's G*H query heads
 // are the MMA's B operand (N = 256).  Keys stream through 128-key tiles from
 // the union of the group's windows:
-//   warp 0      TMA producer: one 128 x 64-byte box per tile (64-byte swizzle),
-//               rows past S filled with zeros;
-//   warp 1      MMA issuer: loads the tile's 128 scale words (two tiles ahead),
-//               writes them in the 32x16-byte scale-factor layout, tcgen05.cp to
-//               TMEM, and two tcgen05.mma kind::mxf4 (K = 64 each) into a
-//               128 x 256 fp32 accumulator;
+//   warp 0      producer: one 128 x 64-byte TMA box per tile (64-byte swizzle,
+//               rows past S filled with zeros) and the tile's 128 key scale
+//               words by 4-byte cp.async straight into the 32x16-byte
+//               scale-factor layout, all completing on the stage's barrier;
+//   warp 1      MMA issuer: tcgen05.cp of the tile's scale factors to one of
+//               two TMEM slots (before it waits for the accumulator), then two
+//               tcgen05.mma kind::mxf4 (K = 64 each) into a 128 x 256 fp32
+//               accumulator;
 //   warps 2-17  epilogue: TMEM lane = key; the four warps on a lane quarter
 //               split the G queries; w * max(0, .) summed over heads, masked
 //               to each query's window.
@@ -46,7 +48,7 @@ constexpr int kEpiWarps = 16;
 
 constexpr int kTkBins = 1024;      // candidate histogram: top 10 key bits
 constexpr int kTkShift = 22;
-constexpr int kTkEvery = 4;        // tiles between threshold updates
+constexpr int kTkEvery = 8;        // tiles between threshold updates (per query pair)
 
 // shared memory of the candidate state, per query of the group
 struct TopkState {
@@ -59,7 +61,7 @@ struct TopkState {
 struct MqaLayout {
   static constexpr uint32_t kAccCol = 0;            // 256 fp32 columns
   static constexpr uint32_t kSfbCol = kN;           // 8 columns (two 128-row atoms)
-  static constexpr uint32_t kSfaCol = kN + 8;       // 4 columns
+  static constexpr uint32_t kSfaCol = kN + 8;       // 2 x 4 columns (tiles alternate)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kA = 0;                                        // stages x 8192
   static constexpr size_t kB = kA + (size_t)kMqaStages * kTileValBytes;  // 256 x 64
@@ -74,18 +76,27 @@ struct MqaLayout {
 };
 
 // The threshold of query q: the lower edge of the highest bin b with
-// count(bins >= b) >= k, or 0 while fewer than k are admitted.  One warp.
+// count(bins >= b) >= k, or 0 while fewer than k are admitted.  One warp;
+// lane l reads bins [32 (31 - l), 32 (32 - l)) with eight 16-byte loads (the
+// counts may be stale, never over-counted: the threshold can only be low).
 __device__ __forceinline__ void update_tau(TopkState& ts, uint32_t k) {
   const int lane = threadIdx.x & 31;
-  // lane l sums bins [kTkBins - 32 (l + 1), kTkBins - 32 l), the top ones first
-  const volatile uint32_t* h = ts.hist;
-  uint32_t c[32];
+  uint32_t c[32];  // c[i]: bin 32 (32 - lane) - 1 - i (highest first)
   uint32_t sum = 0;
+  const uint32_t base = 32u * (31u - (uint32_t)lane);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    c[i] = h[kTkBins - 1 - 32 * lane - i];
-    sum += c[i];
+  for (int v = 0; v < 8; ++v) {
+    uint4 q;
+    asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                 : "r"(smem_u32(ts.hist + base + 4 * v)));
+    c[31 - 4 * v] = q.x;
+    c[30 - 4 * v] = q.y;
+    c[29 - 4 * v] = q.z;
+    c[28 - 4 * v] = q.w;
   }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) sum += c[i];
   uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -97,7 +108,7 @@ __device__ __forceinline__ void update_tau(TopkState& ts, uint32_t k) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (run < k && k <= run + c[i]) {
-        const uint32_t t = (uint32_t)(kTkBins - 1 - 32 * lane - i) << kTkShift;
+        const uint32_t t = (base + 31u - (uint32_t)i) << kTkShift;
         if (t > ts.tau) ts.tau = t;
       }
       run += c[i];
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMqaStages; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + 32);
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(tfull, 1);
@@ -205,24 +216,39 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
   const int n_tiles = tile_hi - tile_lo;
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
-    if (lane == 0 && n_tiles > 0) {
-      tma_prefetch_desc(&tm_k);
+    // ---------------------------------------------------------- producer
+    if (n_tiles > 0) {
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      const uint32_t* ksc = reinterpret_cast<const uint32_t*>(p.k_scales);
+      const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % kMqaStages;
-        if (!mbar_wait(empty_bar(s), ((i / kMqaStages) & 1) ^ 1, abort)) {
-          flag_timeout(p.errors, kTimeoutProducer);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ((i / kMqaStages) & 1) ^ 1, abort))) {
+          if (lane == 0) flag_timeout(p.errors, kTimeoutProducer);
           break;
         }
-        mbar_arrive_expect_tx(full_bar(s), kTileValBytes);
-        tma_load_2d(smem_u32(sA + (size_t)s * kTileValBytes), &tm_k, 0,
-                    (tile_lo + i) * kTileKeys, full_bar(s));
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), kTileValBytes);
+          tma_load_2d(smem_u32(sA + (size_t)s * kTileValBytes), &tm_k, 0,
+                      (tile_lo + i) * kTileKeys, full_bar(s));
+        }
+        const uint32_t dst = smem_u32(sSfa + (size_t)s * 512);
+        const int64_t k0 = (int64_t)(tile_lo + i) * kTileKeys + lane;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          // keys past S (zero values from the TMA fill) take the last key's scales
+          const int64_t kk = k0 + 32 * u < p.S ? k0 + 32 * u : p.S - 1;
+          cp_async_4(dst + 16 * lane + 4 * u, ksc + kk, pol);
+        }
+        cp_async_arrive_noinc(full_bar(s));
         ++issued;
       }
-      for (int i = issued > kMqaStages ? issued - kMqaStages : 0; i < issued; ++i)
-        if (!mbar_wait_drain(full_bar(i % kMqaStages), (i / kMqaStages) & 1))
-          flag_timeout(p.errors, kTimeoutDrain);
+      cp_async_wait_all();
+      if (lane == 0)
+        for (int i = issued > kMqaStages ? issued - kMqaStages : 0; i < issued; ++i)
+          if (!mbar_wait_drain(full_bar(i % kMqaStages), (i / kMqaStages) & 1))
+            flag_timeout(p.errors, kTimeoutDrain);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -233,43 +259,29 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
       tmem_cp_32x128b_x4(sfb_t + 4, smem_desc(smem_u32(sSfb + 512), 16, 128, kLayoutNone));
     }
     __syncwarp();
-    const uint32_t* ksc = reinterpret_cast<const uint32_t*>(p.k_scales);
-    auto load_scales = [&](int i) {
-      uint4 r = make_uint4(0, 0, 0, 0);
-      if (i < n_tiles) {
-        const int64_t k0 = (int64_t)(tile_lo + i) * kTileKeys + lane;
-        r.x = k0 < p.S ? __ldg(ksc + k0) : 0u;
-        r.y = k0 + 32 < p.S ? __ldg(ksc + k0 + 32) : 0u;
-        r.z = k0 + 64 < p.S ? __ldg(ksc + k0 + 64) : 0u;
-        r.w = k0 + 96 < p.S ? __ldg(ksc + k0 + 96) : 0u;
-      }
-      return r;
-    };
-    uint4 sc_next = load_scales(0);
-    uint4 sc_next2 = load_scales(1);
     const uint64_t b_desc = smem_desc(smem_u32(sB), 16, 512, kLayoutSw64);
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i % kMqaStages;
-      const uint4 sc = sc_next;
-      sc_next = sc_next2;
-      sc_next2 = load_scales(i + 2);
-      const bool ok = mbar_wait(full_bar(s), (i / kMqaStages) & 1, abort) &&
-                      mbar_wait(tempty, (i & 1) ^ 1, abort);
-      if (!ok) {
+      if (!mbar_wait(full_bar(s), (i / kMqaStages) & 1, abort)) {
+        if (lane == 0) flag_timeout(p.errors, kTimeoutMma);
+        break;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const uint32_t sfa_i = sfa_t + 4u * (uint32_t)(i & 1);
+      if (lane == 0)
+        tmem_cp_32x128b_x4(sfa_i, smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
+      if (!mbar_wait(tempty, (i & 1) ^ 1, abort)) {
         if (lane == 0) flag_timeout(p.errors, kTimeoutMma);
         break;
       }
       tc_fence_after();
-      *reinterpret_cast<uint4*>(sSfa + (size_t)s * 512 + 16 * lane) = sc;
-      fence_proxy_async_smem();
-      __syncwarp();
       if (lane == 0) {
-        tmem_cp_32x128b_x4(sfa_t, smem_desc(smem_u32(sSfa + (size_t)s * 512), 16, 128, kLayoutNone));
         const uint64_t a_desc =
             smem_desc(smem_u32(sA + (size_t)s * kTileValBytes), 16, 512, kLayoutSw64);
-        mma_mxf4(tmem + Lay::kAccCol, a_desc, b_desc, mxf4_idesc(kN, 0, 0), sfa_t, sfb_t, 0u);
-        mma_mxf4(tmem + Lay::kAccCol, a_desc + 2, b_desc + 2, mxf4_idesc(kN, 2, 2), sfa_t, sfb_t,
+        mma_mxf4(tmem + Lay::kAccCol, a_desc, b_desc, mxf4_idesc(kN, 0, 0), sfa_i, sfb_t, 0u);
+        mma_mxf4(tmem + Lay::kAccCol, a_desc + 2, b_desc + 2, mxf4_idesc(kN, 2, 2), sfa_i, sfb_t,
                  1u);
         mma_commit(empty_bar(s));
         mma_commit(tfull);
@@ -301,8 +313,10 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
       float d[GH * H];
 #pragma unroll
       for (int part = 0; part < GH * H / 32; ++part)
-        tmem_ld32_sync(lane_addr + Lay::kAccCol + (uint32_t)(half * GH * H + 32 * part),
-                       *reinterpret_cast<float(*)[32]>(&d[32 * part]));
+        tmem_ld32(lane_addr + Lay::kAccCol + (uint32_t)(half * GH * H + 32 * part),
+                  *reinterpret_cast<float(*)[32]>(&d[32 * part]));
+      tmem_wait_ld();
+      tmem_take(d);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
@@ -324,11 +338,16 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
             uint32_t base = 0;
             if (lane == 0) base = atomicAdd(&ts.cnt, (uint32_t)__popc(ballot));
             base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            // the histogram: one shared atomic per distinct bin of the warp
+            // (a warp's logits share a few bins; per-lane atomics would
+            // serialise on one address)
+            const uint32_t bin = kk >> kTkShift;
+            const uint32_t same = __match_any_sync(0xFFFFFFFFu, take ? bin : 0xFFFFFFFFu);
             if (take) {
               const int64_t slot = t * p.cand_ld + base + __popc(ballot & ((1u << lane) - 1u));
               p.cand_vals[slot] = logit[j];
               p.cand_idx[slot] = (int32_t)(key - st[j]);
-              atomicAdd(&ts.hist[kk >> kTkShift], 1u);
+              if (lane == __ffs(same) - 1) atomicAdd(&ts.hist[bin], (uint32_t)__popc(same));
             }
           }
         } else {
@@ -339,8 +358,9 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
             row[key] = -INFINITY;
         }
       }
-      // one warp per query pair (its lane quarter 0) raises the thresholds
-      if (TOPK && quarter == 0 && (i % kTkEvery) == kTkEvery - 1) {
+      // one warp of the query pair raises the thresholds every kTkEvery
+      // tiles, the four lane quarters' warps taking turns
+      if (TOPK && (i % kTkEvery) == kTkEvery - 1 && ((i / kTkEvery) & 3) == quarter) {
 #pragma unroll
         for (int j = 0; j < GH; ++j) update_tau(tks[half * GH + j], (uint32_t)p.topk);
       }

@@ -2,11 +2,13 @@
 // the scoring pass of logits + top-k): each CTA loops over work items
 // (sequence b, chunk of tiles_per_item 128-key tiles) with four warp roles:
 //   warps 0-3   epilogue: one thread per key (TMEM lane) loads its row of D and
-//               hands the next_n*H dot products to the epilogue policy `Ep`;
+//               hands the next_n*H dot products to the epilogue policy `Ep`
+//               (at N = 128, warps 0-7, each with one query's 64 columns);
 //   warp 4      MMA issuer: tcgen05.cp of the tile's key scale factors to TMEM
 //               and two tcgen05.mma kind::mxf4 block-scaled MMAs (K = 64 each)
 //               giving D[key, j*H + h] in TMEM (fp32);
-//   warp 5      item loader: picks the next item (a fixed chunk-major
+//   warp 5      item loader (the warp numbers of these roles shift by four at
+//               N = 128): picks the next item (a fixed chunk-major
 //               round-robin, or a global counter when `dynamic`), stages the
 //               sequence's query heads (the MMA's B operand, N = next_n*H), their
 //               scale factors, weights and the chunk's page ids into one of two
@@ -29,8 +31,6 @@
 
 namespace idx {
 
-constexpr int kPagedThreads = 256;
-constexpr int kEpiThreads = 128;
 constexpr int kCopyThreads = 64;
 constexpr int kTileKeys = 128;        // MMA M: two pages
 constexpr int kTileValBytes = kTileKeys * kValBytes;  // 8192
@@ -49,6 +49,12 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 // epilogue needs the registers of a whole SM) one of 20.
 __host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 32 ? 3 : nh == 64 ? 2 : 1; }
 __host__ __device__ constexpr int paged_stages(int nh) { return nh == 32 ? 7 : nh == 64 ? 10 : 20; }
+// Epilogue warps: four (one per TMEM lane quarter) take all N columns of their
+// keys; at N = 128 (one CTA per SM) eight, a pair per lane quarter, each
+// taking one query's 64 heads, so that each SM sub-partition has two warps
+// forming sums.  Then the MMA warp, the item loader and two copy producers.
+__host__ __device__ constexpr int paged_epi_warps(int nh) { return nh == 128 ? 8 : 4; }
+__host__ __device__ constexpr int paged_threads(int nh) { return 32 * (paged_epi_warps(nh) + 4); }
 
 struct ItemDesc {
   int64_t L;        // context length after validation
@@ -62,8 +68,11 @@ struct ItemDesc {
 template <int NH>
 struct PagedLayout {
   static constexpr int kStages = paged_stages(NH);
-  // accumulators: as many as fit the TMEM share of a CTA (512 columns per SM)
-  static constexpr int kAccBufs = NH == 32 ? 3 : 2;
+  // accumulators: as many as fit the TMEM share of a CTA (512 columns per SM:
+  // 128 for each of three N = 32 CTAs, 256 for each of two N = 64 CTAs, all
+  // for one N = 128 CTA); three in every case, so that three tiles' MMAs can
+  // be in flight while the epilogue reads a fourth's
+  static constexpr int kAccBufs = 3;
   static constexpr uint32_t kSfbCol = kAccBufs * NH;        // 2 x 4 columns
   static constexpr uint32_t kSfaCol = kSfbCol + 8;          // 4 columns per accumulator
   static constexpr uint32_t kTmemCols = tmem_cols_for(kSfaCol + 4 * kAccBufs);
@@ -195,10 +204,10 @@ __device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatil
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int part = lane & 15;
   const int64_t cap = (int64_t)p.max_blocks * kPage;
-  const int64_t stride = (int64_t)gridDim.x * (kPagedThreads / 16);
+  const int64_t stride = (int64_t)gridDim.x * (blockDim.x / 16);
   // whole warps stay converged through the encoder's shuffles: a group past
   // the end encodes zeros and stores nothing
-  for (int64_t base = ((int64_t)blockIdx.x * (kPagedThreads / 32) + warp) * 2; base < n_vec;
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x / 32) + warp) * 2; base < n_vec;
        base += stride) {
     const int64_t v = base + (lane >> 4);
     uint4 raw = make_uint4(0, 0, 0, 0);
@@ -252,9 +261,10 @@ __device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatil
   return *abort == 0;
 }
 
-// Barrier among the four epilogue warps only.
+// Barrier among the epilogue warps only.
+template <int EPI_THREADS>
 __device__ __forceinline__ void epilogue_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
 }
 
 template <int H, int NEXT_N, class Ep, bool STEP = false>
@@ -265,6 +275,9 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   using Lay = PagedLayout<NH>;
   constexpr int ACC = Lay::kAccBufs;
   constexpr int kStages = Lay::kStages;
+  constexpr int EPI = paged_epi_warps(NH);   // warps [0, EPI): epilogue
+  constexpr int kMmaWarp = EPI, kLoaderWarp = EPI + 1, kCopyWarp0 = EPI + 2;
+  constexpr int kThreads = paged_threads(NH);
   static_assert(NH % 32 == 0 && NH <= 128, "N must be 32, 64 or 128");
   static_assert(Lay::kTmemCols * paged_ctas_per_sm(NH) <= 512, "TMEM over-subscribed");
 
@@ -291,7 +304,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
     tmem_relinquish();
   }
@@ -302,11 +315,11 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), EPI);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(qfull_bar(q), 1);
-      mbar_init(qempty_bar(q), 1 + 4);  // the MMA commit + the four epilogue warps
+      mbar_init(qempty_bar(q), 1 + EPI);  // the MMA commit + the epilogue warps
     }
     *abort = 0;
     fence_mbar_init();
@@ -359,11 +372,11 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   // The loader's first item is this CTA's own index: its operands are read
   // now, for all of the item's tiles, while the block fills the context-length
   // cache that decides how many of them are used.
-  const bool preloaded = warp == 5 && (int64_t)blockIdx.x < (int64_t)p.B * p.chunks;
+  const bool preloaded = warp == kLoaderWarp && (int64_t)blockIdx.x < (int64_t)p.B * p.chunks;
   if (preloaded)
     load_operands((int32_t)(blockIdx.x % p.B),
                   (int64_t)(blockIdx.x / p.B) * p.tiles_per_cta * kTileKeys, p.tiles_per_cta);
-  for (int i = threadIdx.x; i < p.B && i < kClCache; i += kPagedThreads)
+  for (int i = threadIdx.x; i < p.B && i < kClCache; i += kThreads)
     sCl[i] = __ldg(p.context_lens + i);
   Ep::init(extra);
   tc_fence_before();
@@ -373,7 +386,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   const int64_t n_items = (int64_t)p.B * p.chunks;
   if (dynamic && blockIdx.x == 0 && threadIdx.x == 0) install_generation(item_counter, p.item_gen);
 
-  if (warp == 5) {
+  if (warp == kLoaderWarp) {
     // ---------------------------------------------------------- item loader
     constexpr uint32_t kAll = 0xFFFFFFFFu;
     int n = 0;
@@ -433,9 +446,9 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
       ++n;
       if (it.n_tiles < 0) break;
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kCopyWarp0) {
     // ---------------------------------------------------------- copy producers
-    const int pt = threadIdx.x - 6 * 32;  // 0..63
+    const int pt = threadIdx.x - kCopyWarp0 * 32;  // 0..63
     // the cache is streamed once per call: its lines go first, so that the
     // logits written meanwhile stay in L2 for whatever reads them next
     const uint64_t pol = l2_evict_first_policy();
@@ -499,7 +512,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     }
     // nothing may still be writing shared memory when the CTA exits
     cp_async_wait_all();
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     int tiles = 0;
     bool ok = true;
@@ -561,20 +574,27 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int quarter = warp;  // warps 0-3: TMEM lanes [32*quarter, 32*quarter + 32)
+    // warp w: TMEM lanes [32 (w % 4), +32) (its keys) and columns
+    // [NC (w / 4), +NC) (queries j0 .. j0 + NJ - 1 of the item's NEXT_N)
+    constexpr int NC = NH * 4 / EPI;
+    constexpr int NJ = NEXT_N * 4 / EPI;
+    static_assert(NC == NJ * H, "an epilogue warp takes whole queries");
+    const int quarter = warp & 3;
+    const int cpart = warp >> 2;
+    const int j0 = cpart * NJ;
     const int m = quarter * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cpart * NC);
     int tiles = 0;
     for (int n = 0;; ++n) {
       const int qb = n & 1;
       // every epilogue warp takes the same branches: a wait that gives up
       // raises *abort, the item loop still runs to its end (later waits return
-      // at once), and the four warps leave together after the barrier
+      // at once), and the epilogue warps leave together after the barrier
       const bool have = __all_sync(0xFFFFFFFFu, mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort));
       const ItemDesc it = sItem[qb];
       const bool stop = !have || it.n_tiles < 0;
       const int n_tiles = stop ? 0 : it.n_tiles;
-      const float* w = sW + qb * NH;
+      const float* w = sW + qb * NH + j0 * H;
       for (int t = 0; t < n_tiles; ++t) {
         const int a = tiles % ACC;
         ++tiles;
@@ -583,19 +603,19 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
           continue;
         }
         tc_fence_after();
-        float d[NH];
+        float d[NC];
 #pragma unroll
-        for (int part = 0; part < NH / 32; ++part)
+        for (int part = 0; part < NC / 32; ++part)
           tmem_ld32_sync(lane_addr + (uint32_t)(a * NH + 32 * part),
                          *reinterpret_cast<float(*)[32]>(&d[32 * part]));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(a));
-        Ep::tile(p, it, w, extra, it.k0 + (int64_t)t * kTileKeys + m, d);
+        Ep::template tile<NJ>(p, it, w, extra, it.k0 + (int64_t)t * kTileKeys + m, d, j0);
       }
-      epilogue_sync();
+      epilogue_sync<EPI * 32>();
       if (stop || *abort) break;
-      Ep::item_done(p, it, extra);
+      Ep::item_done(p, it, extra, EPI * 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty_bar(qb));
     }
@@ -603,7 +623,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kTmemCols);
   }

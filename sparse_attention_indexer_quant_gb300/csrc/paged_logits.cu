@@ -25,34 +25,38 @@ struct UnfusedEpilogue {
   static constexpr size_t kExtraSmem = 0;
   __device__ __forceinline__ static void init(uint8_t*) {}
 
-  // Called once per tile by every epilogue thread with its key's NH dot
-  // products (column n = j*H + h).
+  // Called once per tile by every epilogue thread with its key's dot products
+  // for queries j0 .. j0 + NJ - 1 (column n = (j - j0)*H + h; w_smem points at
+  // query j0's weights).
+  template <int NJ>
   __device__ __forceinline__ static void tile(const PagedArgs& p, const ItemDesc& it,
                                               const float* w_smem, uint8_t* /*extra*/,
-                                              int64_t key, const float (&d)[NH]) {
-    float logit[NEXT_N];
-    weighted_relu_sum<H, NEXT_N>(w_smem, d, logit);
+                                              int64_t key, const float (&d)[NJ * H], int j0) {
+    float logit[NJ];
+    weighted_relu_sum<H, NJ>(w_smem, d, logit);
 #pragma unroll
-    for (int j = 0; j < NEXT_N; ++j) {
+    for (int jj = 0; jj < NJ; ++jj) {
+      const int j = j0 + jj;
       const int64_t len = it.L - NEXT_N + j + 1;
       float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
       if (key < len)
-        row[key] = logit[j];
+        row[key] = logit[jj];
       else if (p.clean && key < p.ld)
         row[key] = -INFINITY;
     }
   }
 
-  // -inf into the item's columns that no tile covered (clean rows only).
+  // -inf into the item's columns that no tile covered (clean rows only), by
+  // the epilogue threads [0, epi_threads).
   __device__ __forceinline__ static void item_done(const PagedArgs& p, const ItemDesc& it,
-                                                   uint8_t*) {
+                                                   uint8_t*, int epi_threads) {
     if (!p.clean) return;
     const int64_t lo = it.k0 + (int64_t)it.n_tiles * kTileKeys;
     const int64_t hi = it.k_end < p.ld ? it.k_end : p.ld;
-    const int e = threadIdx.x;  // epilogue threads are warps 0-3
+    const int e = threadIdx.x;
     for (int j = 0; j < NEXT_N; ++j) {
       float* row = p.logits + ((int64_t)it.b * NEXT_N + j) * p.ld;
-      for (int64_t s = lo + e; s < hi; s += kEpiThreads) row[s] = -INFINITY;
+      for (int64_t s = lo + e; s < hi; s += epi_threads) row[s] = -INFINITY;
     }
   }
 };
@@ -61,7 +65,7 @@ struct UnfusedEpilogue {
 // keys and quantises its query heads (decode_step_prologue), launched as a
 // cooperative grid.
 template <int H, int NEXT_N, bool STEP>
-__global__ void __launch_bounds__(kPagedThreads, paged_ctas_per_sm(H * NEXT_N))
+__global__ void __launch_bounds__(paged_threads(H * NEXT_N), paged_ctas_per_sm(H * NEXT_N))
     paged_logits_kernel(const PagedArgs p) {
   paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>, STEP>(
       p, p.kcache, p.item_counter != nullptr, p.clean != 0, p.item_counter);
@@ -80,7 +84,7 @@ int resident_ctas_per_sm(size_t smem, int planned) {
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kPagedThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, paged_threads(H * NEXT_N), smem) !=
             cudaSuccess ||
         n <= 0) {
       (void)cudaGetLastError();
@@ -103,12 +107,14 @@ cudaError_t launch_one(const PagedArgs& a, cudaStream_t stream) {
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (!STEP)
-    return launch_dependent(kern, dim3((unsigned)a.grid), dim3(kPagedThreads), smem, stream, a);
+    return launch_dependent(kern, dim3((unsigned)a.grid), dim3(paged_threads(H * NEXT_N)), smem,
+                            stream, a);
   // the cooperative launch: no more CTAs than the runtime counts as resident
   const int per_sm = resident_ctas_per_sm<H, NEXT_N, STEP>(smem, paged_ctas_per_sm(H * NEXT_N));
   const int64_t cap = (int64_t)(a.sms > 0 ? a.sms : 1) * per_sm;
   const unsigned grid = (unsigned)(a.grid < cap ? a.grid : cap);
-  return launch_dependent_coop(kern, dim3(grid), dim3(kPagedThreads), smem, stream, a);
+  return launch_dependent_coop(kern, dim3(grid), dim3(paged_threads(H * NEXT_N)), smem, stream,
+                               a);
 }
 
 template <bool STEP>

@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   // started after the scoring pass's wait, i.e. after every kernel issued
   // before the call completed
   int64_t L = __ldg(p.context_lens + b);
+  const int64_t cap = (int64_t)p.max_blocks * kPage;
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  int64_t len = L - next_n + j + 1;
+  len = len < 0 ? 0 : len;
   pdl_wait();  // the scoring pass's logits
   // the work-item counter (and the decode step's barrier count) are done
   // with: clear them, so that a replay of this call with the same generation
@@ -78,10 +82,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
     ws.items[0] = 0ull;
     ws.items[1] = 0ull;
   }
-  const int64_t cap = (int64_t)p.max_blocks * kPage;
-  L = L < 0 ? 0 : (L > cap ? cap : L);
-  int64_t len = L - next_n + j + 1;
-  len = len < 0 ? 0 : len;
   // the workspace rows are 256-byte aligned
   cluster_select_row(sm, ws.logits + r * ws.ldw, len, (uint32_t)p.topk, p.out_idx + r * p.topk,
                      parts);

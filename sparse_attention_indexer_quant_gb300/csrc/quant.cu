@@ -130,18 +130,35 @@ __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
       pos = 0;
     }
   }
+  // the thread's four pairs use table columns 4 * part .. 4 * part + 3: one
+  // 16-byte load per table when the four are rotated and the rows aligned
+  float c[4] = {1.f, 1.f, 1.f, 1.f}, s[4] = {0.f, 0.f, 0.f, 0.f};
+  const int col0 = 4 * part;
+  if (live && col0 < half) {
+    const float* c_row = cs + (int64_t)pos * half + col0;
+    const float* s_row = sn + (int64_t)pos * half + col0;
+    if (col0 + 3 < half && ((reinterpret_cast<uintptr_t>(c_row) | reinterpret_cast<uintptr_t>(s_row)) & 15u) == 0) {
+      const float4 cv = __ldg(reinterpret_cast<const float4*>(c_row));
+      const float4 sv = __ldg(reinterpret_cast<const float4*>(s_row));
+      c[0] = cv.x; c[1] = cv.y; c[2] = cv.z; c[3] = cv.w;
+      s[0] = sv.x; s[1] = sv.y; s[2] = sv.z; s[3] = sv.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (col0 + i < half) {
+          c[i] = __ldg(c_row + i);
+          s[i] = __ldg(s_row + i);
+        }
+    }
+  }
   float x[8];
   bf16x8_to_f32(raw, x);
-  const float* c_row = cs + (int64_t)pos * half;
-  const float* s_row = sn + (int64_t)pos * half;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int col = 4 * part + i;  // pair (8 * part + 2i, 8 * part + 2i + 1)
-    if (live && col < half) {
-      const float c = __ldg(c_row + col), s = __ldg(s_row + col);
+    if (col0 + i < half) {  // pair (8 * part + 2i, 8 * part + 2i + 1)
       const float a = x[2 * i], b = x[2 * i + 1];
-      x[2 * i] = __fmaf_rn(a, c, -__fmul_rn(b, s));
-      x[2 * i + 1] = __fmaf_rn(a, s, __fmul_rn(b, c));
+      x[2 * i] = __fmaf_rn(a, c[i], -__fmul_rn(b, s[i]));
+      x[2 * i + 1] = __fmaf_rn(a, s[i], __fmul_rn(b, c[i]));
     }
   }
   uint32_t sw;

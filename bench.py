@@ -953,6 +953,12 @@ def run_case(args):
         ms = time_op(lambda: idx.topk_rows(logits, en_d, TOPK, row_start=st_d, out=out), flush,
                      stream, args.reps)
         print(f"prefill T={T}: topk_rows {ms:.3f} ms")
+        del logits
+        ws = torch.empty(idx.mqa_logits_topk_workspace_bytes(p.T, S, TOPK), dtype=torch.uint8,
+                         device=dev)
+        ms = time_op(lambda: idx.mqa_logits_topk(qv, qs, w, kv, ks, st_d, en_d, p.H, TOPK,
+                                                 workspace=ws, out=out), flush, stream, args.reps)
+        print(f"prefill T={T}: mqa_logits_topk {ms:.3f} ms")
     elif name == "decode":
         p = wl.batched_decode()
         cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)

@@ -148,3 +148,43 @@ def test_topk_many_rows_long_tied_and_unaligned(idx):
         s, n = int(starts[r]), int(lens[r])
         vals = logits[r, s:s + n].astype(np.float64)
         check_topk(out[r], vals, np.zeros_like(vals), n, k, f"row {r} len {n} start {s}")
+
+
+def test_topk_many_rows_patterned_positions(idx):
+    """Rows whose largest values sit in a regular pattern of positions (more
+    rows than SMs, so the one-CTA-per-row kernel runs): large values only in
+    the first 128 of every 2048 positions, small values only there, a rising
+    row, one 2048-block holding the whole top k, and rows of 2 k to 3 k
+    elements.  A select that estimated its threshold from a strided sample of
+    the row would misjudge exactly these."""
+    g = wl.rng(450)
+    k = 2048
+    n_rows = 200
+    kinds = ["high", "low", "rising", "block", "short", "short2"] * 4
+    lens = g.integers(2000, 40000, size=n_rows)
+    ld = int(lens.max())
+    ld += (-ld) % 4
+    logits = np.full((n_rows, ld), np.nan, np.float32)
+    for r in range(n_rows):
+        kind = kinds[r] if r < len(kinds) else "rand"
+        n = int(lens[r])
+        if kind in ("short", "short2"):
+            n = lens[r] = 2 * k + 50 if kind == "short" else 3 * k - 7
+        row = g.standard_normal(n).astype(np.float32)
+        seen = (np.arange(n) % 2048) < 128
+        if kind == "high":
+            row[seen] += 10.0
+        elif kind == "low":
+            row[seen] -= 10.0
+        elif kind == "rising":
+            row = np.arange(n, dtype=np.float32) / 7.0
+        elif kind == "block":
+            b = 2048 * int(g.integers(0, n // 2048))
+            row[b:b + 2048] += 20.0
+        logits[r, :n] = row
+    out = run(idx, logits, np.zeros(n_rows, np.int64), lens, k)
+    for r in list(range(len(kinds))) + [100, 199]:
+        n = int(lens[r])
+        vals = logits[r, :n].astype(np.float64)
+        kind = kinds[r] if r < len(kinds) else "rand"
+        check_topk(out[r], vals, np.zeros_like(vals), n, k, f"row {r} ({kind}) len {n}")

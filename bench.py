@@ -66,9 +66,11 @@ def parse_args():
     ap.add_argument("--case", nargs="+", metavar=("NAME", "T"),
                     help="run one step of the path alone a few times for a profiler and "
                          "print its median time: 'prefill T' (mqa_logits then topk_rows on "
-                         "a T-token causal prefill, H=32), 'decode' (the fused paged "
-                         "logits + top-k of the headline batch), 'quant T' (q-quant and "
-                         "insert of a T-token prefill)")
+                         "a T-token causal prefill, H=32, then the logits + top-k entry), "
+                         "'decode' (the fused paged logits + top-k of the headline batch), "
+                         "'quant T' (q-quant and insert of a T-token prefill), 'next' "
+                         "(q-RoPE + q-quant and K-pool insert of the 32768-token prefill), "
+                         "'step' (the two- and four-launch decode steps)")
     ap.add_argument("--reps", type=int, default=5, help="repetitions of a --case step")
     return ap.parse_args()
 
@@ -986,6 +988,13 @@ def run_case(args):
         slots = torch.from_numpy(p.slots).to(dev)
         ms = time_op(lambda: idx.quant_insert(k, slots, cache), flush, stream, args.reps)
         print(f"prefill T={T}: quant_insert of {k.shape[0]} keys {ms * 1e3:.1f} us")
+    elif name == "next":
+        for key, v in next_entries(idx, dev, flush, stream, args.reps).items():
+            print(f"{key}: {v['workload']}: {v['ms'] * 1e3:.1f} us, {v['frac_of_hbm']:.2f} of HBM")
+    elif name == "step":
+        for key, v in step_entries(idx, dev, flush, stream, args.reps).items():
+            print(f"{key}: two-launch step {v['two_launch_step_us']:.1f} us, four-launch "
+                  f"{v['four_launch_step_us']:.1f} us")
     else:
         raise SystemExit(f"unknown --case {name!r}")
 

@@ -11,9 +11,12 @@
 //     kc[d] = sum_j softmax_j(gate + ape) * k[p - P + 1 + j, d]      (fp32)
 // and kc is quantised to MXFP4 like a key and stored at slot[p].
 //
-// One CTA of 128 threads per batch row: thread d forms kc[d] in two passes
-// over the pool (the maximum, then the exponentials, so no term overflows);
-// the vector goes through shared memory to the encoder's 16-thread layout.
+// One warp per batch row (eight rows per 256-thread CTA); rows that complete
+// no pool leave after reading their slot.  Lane l forms kc for dimensions
+// 4l .. 4l+3 in two passes over the pool (the maximum, then the
+// exponentials, so no term overflows), with 16-byte gate / position-term
+// loads when those arrays allow it; shuffles then give each of the
+// encoder's 16 lanes its eight dimensions.
 #include <math.h>
 
 #include "common.cuh"
@@ -23,51 +26,80 @@
 namespace idx {
 namespace {
 
-constexpr int kPoolThreads = kHeadDim;  // one thread per dimension
+constexpr int kPoolRows = 8;  // rows (warps) per CTA
 
-__global__ void __launch_bounds__(kPoolThreads) kpool_insert_kernel(
+template <bool VEC>
+__device__ __forceinline__ float4 load4(const float* __restrict__ a, int64_t i) {
+  if (VEC) return __ldg(reinterpret_cast<const float4*>(a + i));
+  return make_float4(__ldg(a + i), __ldg(a + i + 1), __ldg(a + i + 2), __ldg(a + i + 3));
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(32 * kPoolRows) kpool_insert_kernel(
     const uint16_t* __restrict__ k, const float* __restrict__ gate, const float* __restrict__ ape,
     const int64_t* __restrict__ slots, int64_t n, int32_t P, uint8_t* __restrict__ cache,
     int64_t num_slots, float* __restrict__ pooled, idx_device_errors* errors) {
-  __shared__ __align__(16) float kc_s[kHeadDim];
-  const int64_t p = blockIdx.x;
-  const int d = threadIdx.x;
+  const int64_t p = (int64_t)blockIdx.x * kPoolRows + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
   pdl_launch_dependents();
   pdl_wait();  // inputs may come from the previous kernel
+  if (p >= n) return;
   const int64_t slot = __ldg(slots + p);
   if (slot < 0 || p < P - 1) return;  // not a pool completion in this batch
   if (slot >= num_slots) {
-    if (d == 0) count_bad_input(errors);
+    if (lane == 0) count_bad_input(errors);
     return;
   }
   const int64_t r0 = p - P + 1;  // the pool's first row
-  float m = -INFINITY;
-  for (int j = 0; j < P; ++j)
-    m = fmaxf(m, __ldg(gate + (r0 + j) * kHeadDim + d) + __ldg(ape + (int64_t)j * kHeadDim + d));
-  float den = 0.f, num = 0.f;
+  const int d0 = 4 * lane;
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   for (int j = 0; j < P; ++j) {
-    const float e =
-        expf(__ldg(gate + (r0 + j) * kHeadDim + d) + __ldg(ape + (int64_t)j * kHeadDim + d) - m);
-    const float kv = __uint_as_float((uint32_t)__ldg(k + (r0 + j) * kHeadDim + d) << 16);
-    den += e;
-    num = fmaf(e, kv, num);
+    const float4 g = load4<VEC>(gate, (r0 + j) * kHeadDim + d0);
+    const float4 a = load4<VEC>(ape, (int64_t)j * kHeadDim + d0);
+    m[0] = fmaxf(m[0], g.x + a.x);
+    m[1] = fmaxf(m[1], g.y + a.y);
+    m[2] = fmaxf(m[2], g.z + a.z);
+    m[3] = fmaxf(m[3], g.w + a.w);
   }
-  const float kc = num / den;
-  if (pooled != nullptr) pooled[p * kHeadDim + d] = kc;
-  kc_s[d] = kc;
-  __syncthreads();
-  if (threadIdx.x >= 32) return;
-  // the first 16 lanes encode the vector (the encoder's shuffles need the
-  // whole warp; lanes 16-31 work on a copy and store nothing)
-  const int part = threadIdx.x & 15;
+  float den[4] = {0.f, 0.f, 0.f, 0.f}, num[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < P; ++j) {
+    const float4 g = load4<VEC>(gate, (r0 + j) * kHeadDim + d0);
+    const float4 a = load4<VEC>(ape, (int64_t)j * kHeadDim + d0);
+    const uint2 kb = __ldg(reinterpret_cast<const uint2*>(k + (r0 + j) * kHeadDim + d0));
+    const float s[4] = {g.x + a.x, g.y + a.y, g.z + a.z, g.w + a.w};
+    const float kv[4] = {__uint_as_float(kb.x << 16), __uint_as_float(kb.x & 0xFFFF0000u),
+                         __uint_as_float(kb.y << 16), __uint_as_float(kb.y & 0xFFFF0000u)};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float e = expf(s[q] - m[q]);
+      den[q] += e;
+      num[q] = fmaf(e, kv[q], num[q]);
+    }
+  }
+  float kc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) kc[q] = num[q] / den[q];
+  if (pooled != nullptr) {
+    float* o = pooled + p * kHeadDim + d0;
+    if (VEC) {
+      *reinterpret_cast<float4*>(o) = make_float4(kc[0], kc[1], kc[2], kc[3]);
+    } else {
+      o[0] = kc[0]; o[1] = kc[1]; o[2] = kc[2]; o[3] = kc[3];
+    }
+  }
+  // encoder lane `part` (lanes 16-31 repeat 0-15: the encoder's shuffles
+  // need the whole warp) takes dimensions 8 part .. 8 part + 7 from lanes
+  // 2 part and 2 part + 1
+  const int part = lane & 15;
   float x[8];
-  const float4 lo = *reinterpret_cast<const float4*>(kc_s + 8 * part);
-  const float4 hi = *reinterpret_cast<const float4*>(kc_s + 8 * part + 4);
-  x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
-  x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    x[q] = __shfl_sync(0xFFFFFFFFu, kc[q], 2 * part);
+    x[4 + q] = __shfl_sync(0xFFFFFFFFu, kc[q], 2 * part + 1);
+  }
   uint32_t sw;
   const uint32_t packed = encode8_f32(x, &sw);
-  if (threadIdx.x >= 16) return;
+  if (lane >= 16) return;
   const int64_t page = slot / kPage, off = slot % kPage;
   uint8_t* pg = cache + page * kPageBytes;
   reinterpret_cast<uint32_t*>(pg + off * kValBytes)[part] = packed;
@@ -81,9 +113,16 @@ cudaError_t launch_kpool_insert(const void* k, const float* gate, const float* a
                                 int64_t num_blocks, float* pooled, idx_device_errors* errors,
                                 cudaStream_t stream) {
   if (n < kpool || n == 0) return cudaSuccess;  // no pool completes in this batch
-  return launch_dependent(kpool_insert_kernel, dim3((unsigned)n), dim3(kPoolThreads), 0, stream,
-                          static_cast<const uint16_t*>(k), gate, ape, slots, n, kpool, cache,
-                          num_blocks * kPage, pooled, errors);
+  const bool vec = (reinterpret_cast<uintptr_t>(gate) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(ape) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(pooled) & 15u) == 0;
+  const dim3 grid((unsigned)((n + kPoolRows - 1) / kPoolRows));
+  const uint16_t* kb = static_cast<const uint16_t*>(k);
+  if (vec)
+    return launch_dependent(kpool_insert_kernel<true>, grid, dim3(32 * kPoolRows), 0, stream, kb,
+                            gate, ape, slots, n, kpool, cache, num_blocks * kPage, pooled, errors);
+  return launch_dependent(kpool_insert_kernel<false>, grid, dim3(32 * kPoolRows), 0, stream, kb,
+                          gate, ape, slots, n, kpool, cache, num_blocks * kPage, pooled, errors);
 }
 
 }  // namespace idx

@@ -106,11 +106,16 @@ __global__ void __launch_bounds__(kBlockThreads) quant_q_kernel(const uint16_t* 
 // y*sin and y*cos rounded first and then one fused multiply-add each, and the
 // 16 threads of the vector encode the result.  A token whose position is
 // outside the table is skipped (its rows are not written) and counted.
+// A group takes VPG consecutive vectors (usually heads of one token): all of
+// their query loads and positions are issued first, then all of their table
+// loads (one 16-byte load per table and vector for a thread whose four pairs
+// are rotated), so that a thread waits for two round trips per VPG vectors.
+template <int VPG>
 __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
     const uint16_t* __restrict__ q, int64_t T, int32_t H, const int32_t* __restrict__ positions,
     const float* __restrict__ cs, const float* __restrict__ sn, int32_t num_pos, int32_t rot_dim,
     uint8_t* __restrict__ vals, uint8_t* __restrict__ scales, idx_device_errors* errors) {
-  const int64_t vec = (int64_t)blockIdx.x * kVecsPerBlock + threadIdx.x / kThreadsPerVec;
+  const int64_t vec0 = ((int64_t)blockIdx.x * kVecsPerBlock + threadIdx.x / kThreadsPerVec) * VPG;
   const int part = threadIdx.x % kThreadsPerVec;
   const int64_t rows = T * H;
   const int half = rot_dim / 2;
@@ -118,54 +123,75 @@ __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
   pdl_wait();  // inputs may come from the previous kernel
   // whole warps stay converged through the shuffles: rows past the end and
   // tokens off the table run the arithmetic on zeros and skip the stores
-  uint4 raw = make_uint4(0, 0, 0, 0);
-  int32_t pos = 0;
-  bool live = vec < rows;
-  if (live) {
-    raw = __ldg(reinterpret_cast<const uint4*>(q + vec * kHeadDim) + part);
-    pos = half > 0 ? __ldg(positions + vec / H) : 0;  // no table without rotated pairs
-    if (half > 0 && (pos < 0 || pos >= num_pos)) {
-      if (part == 0 && vec % H == 0) count_bad_input(errors);
-      live = false;
-      pos = 0;
+  const int64_t t0 = vec0 / H;
+  const int32_t h0 = (int32_t)(vec0 - t0 * H);
+  uint4 raw[VPG];
+  int32_t pos[VPG];
+  bool live[VPG];
+#pragma unroll
+  for (int u = 0; u < VPG; ++u) {
+    const int64_t vec = vec0 + u;
+    live[u] = vec < rows;
+    raw[u] = make_uint4(0, 0, 0, 0);
+    pos[u] = 0;
+    if (live[u]) {
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(q + vec * kHeadDim) + part);
+      // no table without rotated pairs
+      if (half > 0) pos[u] = __ldg(positions + t0 + (h0 + u) / H);
     }
   }
-  // the thread's four pairs use table columns 4 * part .. 4 * part + 3: one
-  // 16-byte load per table when the four are rotated and the rows aligned
-  float c[4] = {1.f, 1.f, 1.f, 1.f}, s[4] = {0.f, 0.f, 0.f, 0.f};
   const int col0 = 4 * part;
-  if (live && col0 < half) {
-    const float* c_row = cs + (int64_t)pos * half + col0;
-    const float* s_row = sn + (int64_t)pos * half + col0;
-    if (col0 + 3 < half && ((reinterpret_cast<uintptr_t>(c_row) | reinterpret_cast<uintptr_t>(s_row)) & 15u) == 0) {
-      const float4 cv = __ldg(reinterpret_cast<const float4*>(c_row));
-      const float4 sv = __ldg(reinterpret_cast<const float4*>(s_row));
-      c[0] = cv.x; c[1] = cv.y; c[2] = cv.z; c[3] = cv.w;
-      s[0] = sv.x; s[1] = sv.y; s[2] = sv.z; s[3] = sv.w;
-    } else {
+  float c[VPG][4], s[VPG][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (col0 + i < half) {
-          c[i] = __ldg(c_row + i);
-          s[i] = __ldg(s_row + i);
-        }
+  for (int u = 0; u < VPG; ++u) {
+    if (live[u] && half > 0 && (pos[u] < 0 || pos[u] >= num_pos)) {
+      if (part == 0 && (h0 + u) % H == 0) count_bad_input(errors);
+      live[u] = false;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      c[u][i] = 1.f;
+      s[u][i] = 0.f;
+    }
+    // the thread's four pairs use table columns 4 * part .. 4 * part + 3
+    if (live[u] && col0 < half) {
+      const float* c_row = cs + (int64_t)pos[u] * half + col0;
+      const float* s_row = sn + (int64_t)pos[u] * half + col0;
+      if (col0 + 3 < half &&
+          ((reinterpret_cast<uintptr_t>(c_row) | reinterpret_cast<uintptr_t>(s_row)) & 15u) == 0) {
+        const float4 cv = __ldg(reinterpret_cast<const float4*>(c_row));
+        const float4 sv = __ldg(reinterpret_cast<const float4*>(s_row));
+        c[u][0] = cv.x; c[u][1] = cv.y; c[u][2] = cv.z; c[u][3] = cv.w;
+        s[u][0] = sv.x; s[u][1] = sv.y; s[u][2] = sv.z; s[u][3] = sv.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (col0 + i < half) {
+            c[u][i] = __ldg(c_row + i);
+            s[u][i] = __ldg(s_row + i);
+          }
+      }
     }
   }
-  float x[8];
-  bf16x8_to_f32(raw, x);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (col0 + i < half) {  // pair (8 * part + 2i, 8 * part + 2i + 1)
-      const float a = x[2 * i], b = x[2 * i + 1];
-      x[2 * i] = __fmaf_rn(a, c[i], -__fmul_rn(b, s[i]));
-      x[2 * i + 1] = __fmaf_rn(a, s[i], __fmul_rn(b, c[i]));
+  for (int u = 0; u < VPG; ++u) {
+    float x[8];
+    bf16x8_to_f32(raw[u], x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (col0 + i < half) {  // pair (8 * part + 2i, 8 * part + 2i + 1)
+        const float a = x[2 * i], b = x[2 * i + 1];
+        x[2 * i] = __fmaf_rn(a, c[u][i], -__fmul_rn(b, s[u][i]));
+        x[2 * i + 1] = __fmaf_rn(a, s[u][i], __fmul_rn(b, c[u][i]));
+      }
     }
+    uint32_t sw;
+    const uint32_t packed = encode8_f32(x, &sw);
+    if (!live[u]) continue;
+    const int64_t vec = vec0 + u;
+    reinterpret_cast<uint32_t*>(vals + vec * kValBytes)[part] = packed;
+    if (part == 0) reinterpret_cast<uint32_t*>(scales)[vec] = sw;
   }
-  uint32_t sw;
-  const uint32_t packed = encode8_f32(x, &sw);
-  if (!live) return;
-  reinterpret_cast<uint32_t*>(vals + vec * kValBytes)[part] = packed;
-  if (part == 0) reinterpret_cast<uint32_t*>(scales)[vec] = sw;
 }
 
 }  // namespace
@@ -176,10 +202,18 @@ cudaError_t launch_rope_quant_q(const void* q, int64_t T, int32_t H, const int32
                                 idx_device_errors* errors, cudaStream_t stream) {
   const int64_t rows = T * H;
   if (rows == 0) return cudaSuccess;
+  const uint16_t* qb = static_cast<const uint16_t*>(q);
+  if (rows >= kBigRows) {
+    const int64_t per_block = (int64_t)kVecsPerBlock * kBigVpg;
+    return launch_dependent(rope_quant_q_kernel<kBigVpg>,
+                            dim3((unsigned)((rows + per_block - 1) / per_block)),
+                            dim3(kBlockThreads), 0, stream, qb, T, H, positions, cs, sn, num_pos,
+                            rot_dim, vals, scales, errors);
+  }
   const int64_t blocks = (rows + kVecsPerBlock - 1) / kVecsPerBlock;
-  return launch_dependent(rope_quant_q_kernel, dim3((unsigned)blocks), dim3(kBlockThreads), 0,
-                          stream, static_cast<const uint16_t*>(q), T, H, positions, cs, sn,
-                          num_pos, rot_dim, vals, scales, errors);
+  return launch_dependent(rope_quant_q_kernel<1>, dim3((unsigned)blocks), dim3(kBlockThreads), 0,
+                          stream, qb, T, H, positions, cs, sn, num_pos, rot_dim, vals, scales,
+                          errors);
 }
 
 cudaError_t launch_quant_insert(const void* k, int64_t n_tokens, int64_t row_stride,

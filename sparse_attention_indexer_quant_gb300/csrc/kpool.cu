@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(32 * kPoolRows) kpool_insert_kernel(
   const int d0 = 4 * lane;
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   for (int j = 0; j < P; ++j) {
+    // the second pass's keys start on their way to L1 with the first pass's loads
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(k + (r0 + j) * kHeadDim + d0));
     const float4 g = load4<VEC>(gate, (r0 + j) * kHeadDim + d0);
     const float4 a = load4<VEC>(ape, (int64_t)j * kHeadDim + d0);
     m[0] = fmaxf(m[0], g.x + a.x);

@@ -106,10 +106,60 @@ __global__ void __launch_bounds__(kBlockThreads) quant_q_kernel(const uint16_t* 
 // y*sin and y*cos rounded first and then one fused multiply-add each, and the
 // 16 threads of the vector encode the result.  A token whose position is
 // outside the table is skipped (its rows are not written) and counted.
-// A group takes VPG consecutive vectors (usually heads of one token): all of
-// their query loads and positions are issued first, then all of their table
-// loads (one 16-byte load per table and vector for a thread whose four pairs
-// are rotated), so that a thread waits for two round trips per VPG vectors.
+// A group takes VPG consecutive vectors: all of their query loads are issued
+// first, then the table loads, so that a thread waits for two round trips per
+// VPG vectors.  When VPG divides H (every group holds heads of one token),
+// the group reads the token's position and table row once.
+__device__ __forceinline__ void rope_table(const float* __restrict__ cs,
+                                           const float* __restrict__ sn, int32_t pos, int half,
+                                           int col0, float (&c)[4], float (&s)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    c[i] = 1.f;
+    s[i] = 0.f;
+  }
+  if (col0 >= half) return;  // the thread's four pairs use table columns col0 .. col0 + 3
+  const float* c_row = cs + (int64_t)pos * half + col0;
+  const float* s_row = sn + (int64_t)pos * half + col0;
+  if (col0 + 3 < half &&
+      ((reinterpret_cast<uintptr_t>(c_row) | reinterpret_cast<uintptr_t>(s_row)) & 15u) == 0) {
+    const float4 cv = __ldg(reinterpret_cast<const float4*>(c_row));
+    const float4 sv = __ldg(reinterpret_cast<const float4*>(s_row));
+    c[0] = cv.x; c[1] = cv.y; c[2] = cv.z; c[3] = cv.w;
+    s[0] = sv.x; s[1] = sv.y; s[2] = sv.z; s[3] = sv.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (col0 + i < half) {
+        c[i] = __ldg(c_row + i);
+        s[i] = __ldg(s_row + i);
+      }
+  }
+}
+
+// Turns the thread's pairs and encodes; stores when live.  All 32 lanes call it.
+__device__ __forceinline__ void rope_encode_store(uint4 raw, const float (&c)[4],
+                                                  const float (&s)[4], int half, int part,
+                                                  bool live, int64_t vec, uint8_t* __restrict__ vals,
+                                                  uint8_t* __restrict__ scales) {
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  const int col0 = 4 * part;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (col0 + i < half) {  // pair (8 * part + 2i, 8 * part + 2i + 1)
+      const float a = x[2 * i], b = x[2 * i + 1];
+      x[2 * i] = __fmaf_rn(a, c[i], -__fmul_rn(b, s[i]));
+      x[2 * i + 1] = __fmaf_rn(a, s[i], __fmul_rn(b, c[i]));
+    }
+  }
+  uint32_t sw;
+  const uint32_t packed = encode8_f32(x, &sw);
+  if (!live) return;
+  reinterpret_cast<uint32_t*>(vals + vec * kValBytes)[part] = packed;
+  if (part == 0) reinterpret_cast<uint32_t*>(scales)[vec] = sw;
+}
+
 template <int VPG>
 __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
     const uint16_t* __restrict__ q, int64_t T, int32_t H, const int32_t* __restrict__ positions,
@@ -119,6 +169,7 @@ __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
   const int part = threadIdx.x % kThreadsPerVec;
   const int64_t rows = T * H;
   const int half = rot_dim / 2;
+  const int col0 = 4 * part;
   pdl_launch_dependents();
   pdl_wait();  // inputs may come from the previous kernel
   // whole warps stay converged through the shuffles: rows past the end and
@@ -126,71 +177,41 @@ __global__ void __launch_bounds__(kBlockThreads) rope_quant_q_kernel(
   const int64_t t0 = vec0 / H;
   const int32_t h0 = (int32_t)(vec0 - t0 * H);
   uint4 raw[VPG];
-  int32_t pos[VPG];
-  bool live[VPG];
 #pragma unroll
-  for (int u = 0; u < VPG; ++u) {
-    const int64_t vec = vec0 + u;
-    live[u] = vec < rows;
-    raw[u] = make_uint4(0, 0, 0, 0);
-    pos[u] = 0;
-    if (live[u]) {
-      raw[u] = __ldg(reinterpret_cast<const uint4*>(q + vec * kHeadDim) + part);
-      // no table without rotated pairs
-      if (half > 0) pos[u] = __ldg(positions + t0 + (h0 + u) / H);
+  for (int u = 0; u < VPG; ++u)
+    raw[u] = vec0 + u < rows ? __ldg(reinterpret_cast<const uint4*>(q + (vec0 + u) * kHeadDim) + part)
+                             : make_uint4(0, 0, 0, 0);
+  // a position outside the table: the token's rows are skipped, counted once
+  // (by the group holding its head 0); no table without rotated pairs
+  auto position = [&](int64_t t, int32_t h, bool& live) {
+    if (!live || half == 0) return 0;
+    const int32_t pos = __ldg(positions + t);
+    if (pos < 0 || pos >= num_pos) {
+      if (part == 0 && h == 0) count_bad_input(errors);
+      live = false;
+      return 0;
     }
-  }
-  const int col0 = 4 * part;
-  float c[VPG][4], s[VPG][4];
+    return pos;
+  };
+  if (H % VPG == 0) {  // warp-uniform: every group holds heads h0 .. h0 + VPG - 1 of token t0
+    bool ok = vec0 < rows;
+    const int32_t pos = position(t0, h0, ok);
+    float c[4], s[4];
+    rope_table(cs, sn, pos, ok ? half : 0, col0, c, s);
 #pragma unroll
-  for (int u = 0; u < VPG; ++u) {
-    if (live[u] && half > 0 && (pos[u] < 0 || pos[u] >= num_pos)) {
-      if (part == 0 && (h0 + u) % H == 0) count_bad_input(errors);
-      live[u] = false;
+    for (int u = 0; u < VPG; ++u)
+      rope_encode_store(raw[u], c, s, half, part, ok && vec0 + u < rows, vec0 + u, vals, scales);
+  } else {
+#pragma unroll
+    for (int u = 0; u < VPG; ++u) {
+      const int64_t t = t0 + (h0 + u) / H;
+      const int32_t h = (h0 + u) % H;
+      bool live = vec0 + u < rows;
+      const int32_t pos = position(t, h, live);
+      float c[4], s[4];
+      rope_table(cs, sn, pos, live ? half : 0, col0, c, s);
+      rope_encode_store(raw[u], c, s, half, part, live, vec0 + u, vals, scales);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      c[u][i] = 1.f;
-      s[u][i] = 0.f;
-    }
-    // the thread's four pairs use table columns 4 * part .. 4 * part + 3
-    if (live[u] && col0 < half) {
-      const float* c_row = cs + (int64_t)pos[u] * half + col0;
-      const float* s_row = sn + (int64_t)pos[u] * half + col0;
-      if (col0 + 3 < half &&
-          ((reinterpret_cast<uintptr_t>(c_row) | reinterpret_cast<uintptr_t>(s_row)) & 15u) == 0) {
-        const float4 cv = __ldg(reinterpret_cast<const float4*>(c_row));
-        const float4 sv = __ldg(reinterpret_cast<const float4*>(s_row));
-        c[u][0] = cv.x; c[u][1] = cv.y; c[u][2] = cv.z; c[u][3] = cv.w;
-        s[u][0] = sv.x; s[u][1] = sv.y; s[u][2] = sv.z; s[u][3] = sv.w;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (col0 + i < half) {
-            c[u][i] = __ldg(c_row + i);
-            s[u][i] = __ldg(s_row + i);
-          }
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < VPG; ++u) {
-    float x[8];
-    bf16x8_to_f32(raw[u], x);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (col0 + i < half) {  // pair (8 * part + 2i, 8 * part + 2i + 1)
-        const float a = x[2 * i], b = x[2 * i + 1];
-        x[2 * i] = __fmaf_rn(a, c[u][i], -__fmul_rn(b, s[u][i]));
-        x[2 * i + 1] = __fmaf_rn(a, s[u][i], __fmul_rn(b, c[u][i]));
-      }
-    }
-    uint32_t sw;
-    const uint32_t packed = encode8_f32(x, &sw);
-    if (!live[u]) continue;
-    const int64_t vec = vec0 + u;
-    reinterpret_cast<uint32_t*>(vals + vec * kValBytes)[part] = packed;
-    if (part == 0) reinterpret_cast<uint32_t*>(scales)[vec] = sw;
   }
 }
 

@@ -11,12 +11,14 @@
 //     kc[d] = sum_j softmax_j(gate + ape) * k[p - P + 1 + j, d]      (fp32)
 // and kc is quantised to MXFP4 like a key and stored at slot[p].
 //
-// One warp per batch row (eight rows per 256-thread CTA); rows that complete
-// no pool leave after reading their slot.  Lane l forms kc for dimensions
-// 4l .. 4l+3 in two passes over the pool (the maximum, then the
-// exponentials, so no term overflows), with 16-byte gate / position-term
-// loads when those arrays allow it; shuffles then give each of the
-// encoder's 16 lanes its eight dimensions.
+// One warp per kPoolWarpRows consecutive batch rows (eight warps per CTA): the
+// warp reads their slots at once and forms the pools they complete, one after
+// the other (with pools of 4 or more, at most about one per warp, so the grid
+// is a fraction of the rows and finishes in about one wave).  Lane l forms kc
+// for dimensions 4l .. 4l+3 in two passes over the pool (the maximum, then
+// the exponentials, so no term overflows), with 16-byte gate / position-term
+// loads when those arrays allow it; shuffles then give each of the encoder's
+// 16 lanes its eight dimensions.
 #include <math.h>
 
 #include "common.cuh"
@@ -26,7 +28,8 @@
 namespace idx {
 namespace {
 
-constexpr int kPoolRows = 8;  // rows (warps) per CTA
+constexpr int kPoolWarps = 8;     // warps per CTA
+constexpr int kPoolWarpRows = 4;  // batch rows per warp
 
 template <bool VEC>
 __device__ __forceinline__ float4 load4(const float* __restrict__ a, int64_t i) {
@@ -34,22 +37,13 @@ __device__ __forceinline__ float4 load4(const float* __restrict__ a, int64_t i) 
   return make_float4(__ldg(a + i), __ldg(a + i + 1), __ldg(a + i + 2), __ldg(a + i + 3));
 }
 
+// The pool completed by row p, quantised and stored at `slot`.  All 32 lanes call it.
 template <bool VEC>
-__global__ void __launch_bounds__(32 * kPoolRows) kpool_insert_kernel(
-    const uint16_t* __restrict__ k, const float* __restrict__ gate, const float* __restrict__ ape,
-    const int64_t* __restrict__ slots, int64_t n, int32_t P, uint8_t* __restrict__ cache,
-    int64_t num_slots, float* __restrict__ pooled, idx_device_errors* errors) {
-  const int64_t p = (int64_t)blockIdx.x * kPoolRows + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  pdl_launch_dependents();
-  pdl_wait();  // inputs may come from the previous kernel
-  if (p >= n) return;
-  const int64_t slot = __ldg(slots + p);
-  if (slot < 0 || p < P - 1) return;  // not a pool completion in this batch
-  if (slot >= num_slots) {
-    if (lane == 0) count_bad_input(errors);
-    return;
-  }
+__device__ __forceinline__ void kpool_row(const uint16_t* __restrict__ k,
+                                          const float* __restrict__ gate,
+                                          const float* __restrict__ ape, int64_t p, int32_t P,
+                                          int64_t slot, uint8_t* __restrict__ cache,
+                                          float* __restrict__ pooled, int lane) {
   const int64_t r0 = p - P + 1;  // the pool's first row
   const int d0 = 4 * lane;
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -108,6 +102,30 @@ __global__ void __launch_bounds__(32 * kPoolRows) kpool_insert_kernel(
   if (part == 0) *reinterpret_cast<uint32_t*>(pg + kPageValBytes + off * kScaleBytes) = sw;
 }
 
+template <bool VEC>
+__global__ void __launch_bounds__(32 * kPoolWarps) kpool_insert_kernel(
+    const uint16_t* __restrict__ k, const float* __restrict__ gate, const float* __restrict__ ape,
+    const int64_t* __restrict__ slots, int64_t n, int32_t P, uint8_t* __restrict__ cache,
+    int64_t num_slots, float* __restrict__ pooled, idx_device_errors* errors) {
+  const int64_t p0 = ((int64_t)blockIdx.x * kPoolWarps + threadIdx.x / 32) * kPoolWarpRows;
+  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();  // inputs may come from the previous kernel
+  // lane r < kPoolWarpRows reads row p0 + r's slot; a row completes a pool
+  // in this batch iff its slot is valid and p >= P - 1
+  int64_t slot = -1;
+  const int64_t pr = p0 + lane;
+  if (lane < kPoolWarpRows && pr < n && pr >= P - 1) slot = __ldg(slots + pr);
+  const bool bad = slot >= num_slots;
+  if (bad) count_bad_input(errors);
+  uint32_t todo = __ballot_sync(0xFFFFFFFFu, slot >= 0 && !bad);
+  for (; todo != 0u; todo &= todo - 1u) {
+    const int r = __ffs(todo) - 1;
+    kpool_row<VEC>(k, gate, ape, p0 + r, P, __shfl_sync(0xFFFFFFFFu, slot, r), cache, pooled,
+                   lane);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_kpool_insert(const void* k, const float* gate, const float* ape,
@@ -118,12 +136,13 @@ cudaError_t launch_kpool_insert(const void* k, const float* gate, const float* a
   const bool vec = (reinterpret_cast<uintptr_t>(gate) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(ape) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(pooled) & 15u) == 0;
-  const dim3 grid((unsigned)((n + kPoolRows - 1) / kPoolRows));
+  constexpr int64_t per_cta = (int64_t)kPoolWarps * kPoolWarpRows;
+  const dim3 grid((unsigned)((n + per_cta - 1) / per_cta));
   const uint16_t* kb = static_cast<const uint16_t*>(k);
   if (vec)
-    return launch_dependent(kpool_insert_kernel<true>, grid, dim3(32 * kPoolRows), 0, stream, kb,
+    return launch_dependent(kpool_insert_kernel<true>, grid, dim3(32 * kPoolWarps), 0, stream, kb,
                             gate, ape, slots, n, kpool, cache, num_blocks * kPage, pooled, errors);
-  return launch_dependent(kpool_insert_kernel<false>, grid, dim3(32 * kPoolRows), 0, stream, kb,
+  return launch_dependent(kpool_insert_kernel<false>, grid, dim3(32 * kPoolWarps), 0, stream, kb,
                           gate, ape, slots, n, kpool, cache, num_blocks * kPage, pooled, errors);
 }
 

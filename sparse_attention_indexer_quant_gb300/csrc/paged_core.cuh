@@ -261,10 +261,21 @@ __device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatil
   return *abort == 0;
 }
 
-// Barrier among the epilogue warps only.
-template <int EPI_THREADS>
-__device__ __forceinline__ void epilogue_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+// Barrier among the epilogue warps only, returning pred ORed (AND = false:
+// ANDed) over the epilogue threads, so that every epilogue warp takes the
+// same decision.
+template <int EPI_THREADS, bool AND = false>
+__device__ __forceinline__ bool epilogue_sync_reduce(bool pred) {
+  uint32_t r;
+  if (AND)
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(EPI_THREADS) : "memory");
+  else
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(EPI_THREADS) : "memory");
+  return r != 0;
 }
 
 template <int H, int NEXT_N, class Ep, bool STEP = false>
@@ -587,10 +598,13 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     int tiles = 0;
     for (int n = 0;; ++n) {
       const int qb = n & 1;
-      // every epilogue warp takes the same branches: a wait that gives up
-      // raises *abort, the item loop still runs to its end (later waits return
-      // at once), and the epilogue warps leave together after the barrier
-      const bool have = __all_sync(0xFFFFFFFFu, mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort));
+      // every epilogue warp takes the same branches: the item's wait is
+      // agreed over the epilogue warps, a wait that gives up raises *abort,
+      // the item loop still runs to its end (later waits return at once), and
+      // the epilogue warps leave together, on one agreed decision (two warps
+      // that read *abort apart would otherwise part at the barrier below)
+      const bool have = epilogue_sync_reduce<EPI * 32, true>(
+          mbar_wait(qfull_bar(qb), (n >> 1) & 1, abort));
       const ItemDesc it = sItem[qb];
       const bool stop = !have || it.n_tiles < 0;
       const int n_tiles = stop ? 0 : it.n_tiles;
@@ -613,8 +627,7 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
         if (lane == 0) mbar_arrive(tempty_bar(a));
         Ep::template tile<NJ>(p, it, w, extra, it.k0 + (int64_t)t * kTileKeys + m, d, j0);
       }
-      epilogue_sync<EPI * 32>();
-      if (stop || *abort) break;
+      if (epilogue_sync_reduce<EPI * 32>(stop || *abort)) break;
       Ep::item_done(p, it, extra, EPI * 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty_bar(qb));

@@ -85,6 +85,35 @@ def test_rope_quant_q_positions_off_the_table_are_skipped(idx, oracle):
     assert (v[~ok] == 0x5A).all() and (s[~ok] == 0x5A).all()
 
 
+def test_rope_quant_q_groups_straddling_tokens(idx, oracle):
+    """At 65536 rows and more a 16-thread group quantises four consecutive
+    head rows; with H = 6 a group's rows can belong to two tokens, each with
+    its own table row.  Some positions lie off the table: those tokens'
+    rows stay untouched and each such token is counted once."""
+    T, H = 11003, 6
+    g = wl.rng(7150)
+    q = wl.normal_bf16(g, (T, H, 128))
+    num_pos = 20000
+    cs, sn = _table(num_pos, 32)
+    pos = g.integers(0, num_pos, size=T).astype(np.int32)
+    bad = g.choice(T, 37, replace=False)
+    pos[bad[:20]] = num_pos + g.integers(0, 100, size=20)
+    pos[bad[20:]] = -1 - g.integers(0, 100, size=17)
+    errs = idx.new_errors()
+    vals = torch.full((T * H, 64), 0x5A, dtype=torch.uint8, device="cuda")
+    scl = torch.full((T * H, 4), 0x5A, dtype=torch.uint8, device="cuda")
+    idx.rope_quant_q(dev_bf16(q), dev(pos), dev(cs), dev(sn), 64, out_vals=vals, out_scales=scl,
+                     errors=errs)
+    torch.cuda.synchronize()
+    assert errs.cpu().tolist() == [37, 0]
+    ok = (pos >= 0) & (pos < num_pos)
+    ov, osc, _ = oracle.rope_quant_q(q[ok], pos[ok], cs, sn, 64)
+    v = vals.cpu().numpy().reshape(T, H, 64)
+    sc = scl.cpu().numpy().reshape(T, H, 4)
+    assert np.array_equal(v[ok].reshape(-1, 64), ov) and np.array_equal(sc[ok].reshape(-1, 4), osc)
+    assert (v[~ok] == 0x5A).all() and (sc[~ok] == 0x5A).all()
+
+
 def _pool_batch(seed, n, P, pad_front=0, frac_bad=0.0, num_blocks=64):
     """A prefill-like batch: rows in token order, the last row of every
     complete pool (counted from row pad_front) has a distinct slot, the other
@@ -106,7 +135,8 @@ def _pool_batch(seed, n, P, pad_front=0, frac_bad=0.0, num_blocks=64):
 
 
 @pytest.mark.parametrize("n,P,pad_front", [(1000, 4, 0), (4096, 16, 0), (777, 64, 3),
-                                           (130, 128, 0), (333, 1, 0), (3, 4, 0), (4, 4, 0)])
+                                           (130, 128, 0), (333, 1, 0), (3, 4, 0), (4, 4, 0),
+                                           (4099, 2, 1), (3001, 3, 2)])
 def test_kpool_insert_parity(idx, oracle, n, P, pad_front):
     k, gate, ape, slots = _pool_batch(7300 + n + P, n, P, pad_front)
     cache = dev(wl.poisoned_cache(64))

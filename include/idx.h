@@ -325,9 +325,15 @@ IDX_API idx_status idx_paged_logits_topk_noalloc(
  *   count the new tokens.  out_idx [B*next_n, k] as there.
  *   workspace    at least idx_paged_decode_step_workspace_bytes(...) bytes,
  *                256-byte aligned, no initialisation, not shared by calls that
- *                overlap on the GPU.
- *   The scoring launch is cooperative (every CTA resident at once, for the
- *   grid-wide barrier between the insert and the reads).
+ *                overlap on the GPU.  Besides the fused call's contents it
+ *                holds the quantised query heads, a chunk counter and one
+ *                count per sequence (generation-tagged, cleared by the
+ *                select).
+ *   The scoring launch does the step's quantisation and insert first, in
+ *   small chunks that its CTAs claim from a counter in the workspace; a CTA
+ *   waits for a sequence's chunks to be done before it reads any of the
+ *   sequence's keys (a bounded wait; a wait that gives up sets the timeout
+ *   bit).  The launch needs no co-residency of its CTAs.
  * ------------------------------------------------------------------------ */
 IDX_API size_t idx_paged_decode_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H,
                                              int32_t max_blocks, int32_t page_size, int32_t k);

@@ -61,37 +61,19 @@ struct PagedArgs {
   int32_t wait_first;                // wait for the previous kernel before letting the
                                      // next one start (its early code may read the inputs)
   idx_device_errors* errors;
-  // decode step only (the scoring pass quantises the step's query heads and
-  // inserts its new keys before a grid-wide barrier)
+  // decode step only (the scoring pass quantises each sequence's query heads
+  // and inserts its new keys before any of its items is scored)
   const uint16_t* q_bf16;            // [rows, H, 128] bf16
   const uint16_t* k_new;             // [rows, 128] bf16: row b*next_n + j at position
                                      // L_b - next_n + j of sequence b
-  uint8_t* q_vals_w;                 // == q_vals, written by the prologue
+  uint8_t* q_vals_w;                 // == q_vals, written by the scoring pass
   uint8_t* q_scales_w;               // == q_scales
   uint8_t* kcache_w;                 // == kcache
-  unsigned long long* grid_bar;      // generation-tagged arrival count
+  unsigned long long* seq_state;     // [B] generation-tagged count of a sequence's
+                                     // preparation chunks done; non-null selects the
+                                     // decode step
+  unsigned long long* prep_counter;  // generation-tagged claim counter of the chunks
 };
-
-// Launches kern with programmatic stream serialization and as a cooperative
-// launch: every CTA of the grid is resident at once (the grid-wide barrier of
-// the decode step relies on it).
-template <class... KArgs, class... Args>
-cudaError_t launch_dependent_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                  cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
-}
 
 cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream);
 

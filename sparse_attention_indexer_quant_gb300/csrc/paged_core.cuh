@@ -185,48 +185,70 @@ __device__ __forceinline__ void install_generation(unsigned long long* ctr, unsi
   }
 }
 
-// The decode step's prologue (a scoring pass that also does the step's
-// insert and query quantisation), run by every thread of every CTA before the
-// streaming loop: the grid's 16-thread groups take, in turn, the step's query
-// heads (rows * H vectors, quantised into q_vals_w / q_scales_w) and then its
-// new keys (row b * NEXT_N + j to position L_b - NEXT_N + j of sequence b,
-// through the block table, quantised into the cache), and the grid then meets
-// at a barrier: a generation-tagged arrival count in the workspace (the launch
-// is cooperative, so every CTA is resident), waited on by one thread per CTA
-// for at most kWaitLimitNs.  A new key whose position is outside the block
+// The decode step's preparation (a scoring pass that also does the step's
+// insert and query quantisation), spread over the grid's item loaders: the
+// work is cut into chunks of kStepChunkPasses warp passes (two 128-element
+// vectors a pass: the sequence's NEXT_N * H query heads, then its NEXT_N new
+// keys), B * step_chunks() in all, claimed from a generation-tagged counter
+// in the workspace by each loader before its first item.  A loader that
+// finishes a chunk of sequence b adds one to b's generation-tagged done count;
+// before staging an item of b a loader waits, for at most kWaitLimitNs, until
+// that count reaches b's chunk total.  Every chunk is claimed by a running
+// CTA that waits on nothing while doing it, so the waits need no
+// co-residency of the grid.  A new key whose position is outside the block
 // table or whose page id is outside the cache is skipped and counted.
-// Returns false (and raises *abort) if the barrier gave up.
+constexpr int kStepChunkPasses = 2;
+
 template <int H, int NEXT_N>
-__device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatile int* abort) {
-  const int64_t rows = (int64_t)p.B * NEXT_N;
-  const int64_t n_q = rows * H;
-  const int64_t n_vec = n_q + rows;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+__host__ __device__ constexpr int step_chunks() {
+  return ((NEXT_N * H + NEXT_N + 1) / 2 + kStepChunkPasses - 1) / kStepChunkPasses;
+}
+
+// Chunk ci of sequence b, by the whole loader warp (the encoder's shuffles
+// need converged warps: a 16-lane group past the end encodes zeros and stores
+// nothing).  All of a lane's loads are issued before any is encoded.
+template <int H, int NEXT_N>
+__device__ __forceinline__ void step_prepare_chunk(const PagedArgs& p, int32_t b, int ci,
+                                                   int lane) {
+  constexpr int kQ = NEXT_N * H;
+  constexpr int kB = kStepChunkPasses;
   const int part = lane & 15;
   const int64_t cap = (int64_t)p.max_blocks * kPage;
-  const int64_t stride = (int64_t)gridDim.x * (blockDim.x / 16);
-  // whole warps stay converged through the encoder's shuffles: a group past
-  // the end encodes zeros and stores nothing
-  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x / 32) + warp) * 2; base < n_vec;
-       base += stride) {
-    const int64_t v = base + (lane >> 4);
-    uint4 raw = make_uint4(0, 0, 0, 0);
+  int64_t L = __ldg(p.context_lens + b);
+  L = L < 0 ? 0 : (L > cap ? cap : L);  // (an over-long context is counted by the loop)
+  uint4 raw[kB];
+  int32_t id[kB];
+#pragma unroll
+  for (int u = 0; u < kB; ++u) {
+    const int v = 2 * (ci * kB + u) + (lane >> 4);
+    raw[u] = make_uint4(0, 0, 0, 0);
+    id[u] = -1;
+    if (v < kQ) {
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)b * kQ + v) * kHeadDim) +
+                     part);
+    } else if (v < kQ + NEXT_N) {
+      const int j = v - kQ;
+      const int64_t pos = L - NEXT_N + j;
+      if (pos >= 0) {
+        id[u] = __ldg(p.block_table + (int64_t)b * p.max_blocks + pos / kPage);
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(p.k_new + ((int64_t)b * NEXT_N + j) * kHeadDim) +
+                       part);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kB; ++u) {
+    const int v = 2 * (ci * kB + u) + (lane >> 4);
     uint8_t* vdst = nullptr;
     uint8_t* sdst = nullptr;
-    if (v < n_q) {
-      raw = __ldg(reinterpret_cast<const uint4*>(p.q_bf16 + v * kHeadDim) + part);
-      vdst = p.q_vals_w + v * kValBytes;
-      sdst = p.q_scales_w + v * kScaleBytes;
-    } else if (v < n_vec) {
-      const int64_t r = v - n_q;
-      const int64_t b = r / NEXT_N, j = r % NEXT_N;
-      int64_t L = __ldg(p.context_lens + b);
-      L = L < 0 ? 0 : (L > cap ? cap : L);  // (an over-long context is counted by the loop)
-      const int64_t pos = L - NEXT_N + j;
-      const int32_t id = pos >= 0 ? __ldg(p.block_table + b * p.max_blocks + pos / kPage) : -1;
-      if (pos >= 0 && id >= 0 && id < p.num_blocks) {
-        raw = __ldg(reinterpret_cast<const uint4*>(p.k_new + r * kHeadDim) + part);
-        uint8_t* pg = p.kcache_w + (int64_t)id * kPageBytes;
+    if (v < kQ) {
+      const int64_t row = (int64_t)b * kQ + v;
+      vdst = p.q_vals_w + row * kValBytes;
+      sdst = p.q_scales_w + row * kScaleBytes;
+    } else if (v < kQ + NEXT_N) {
+      const int64_t pos = L - NEXT_N + (v - kQ);
+      if (pos >= 0 && id[u] >= 0 && id[u] < p.num_blocks) {
+        uint8_t* pg = p.kcache_w + (int64_t)id[u] * kPageBytes;
         vdst = pg + (pos % kPage) * kValBytes;
         sdst = pg + kPageValBytes + (pos % kPage) * kScaleBytes;
       } else if (part == 0) {
@@ -234,31 +256,40 @@ __device__ __forceinline__ bool decode_step_prologue(const PagedArgs& p, volatil
       }
     }
     uint32_t sw;
-    const uint32_t packed = encode8(raw, &sw);
+    const uint32_t packed = encode8(raw[u], &sw);
     if (vdst != nullptr) {
       reinterpret_cast<uint32_t*>(vdst)[part] = packed;
       if (part == 0) *reinterpret_cast<uint32_t*>(sdst) = sw;
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    constexpr unsigned long long kCount = (1ull << kItemBits) - 1ull;
-    __threadfence();  // the CTA's writes before its arrival
-    claim_item(p.grid_bar, p.item_gen, p.errors);
+}
+
+// The decode step: by the loader warp, before it stages an item of sequence
+// b, a wait until every chunk of b is done (returns false, raising *abort,
+// if the wait gives up).
+template <int H, int NEXT_N>
+__device__ __forceinline__ bool step_wait_sequence(const PagedArgs& p, int32_t b, int lane,
+                                                   volatile int* abort) {
+  constexpr unsigned long long kCount = (1ull << kItemBits) - 1ull;
+  uint32_t ok = 1;
+  if (lane == 0) {
+    const unsigned long long* st = p.seq_state + b;
     const unsigned long long t0 = global_timer_ns();
-    while (true) {
+    for (uint32_t it = 0;; ++it) {
       unsigned long long c;
-      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(p.grid_bar) : "memory");
-      if ((c >> kItemBits) == p.item_gen && (c & kCount) >= gridDim.x) break;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(st) : "memory");
+      if ((c >> kItemBits) == p.item_gen && (c & kCount) >= (unsigned long long)step_chunks<H, NEXT_N>())
+        break;
+      if ((it & 15u) == 15u && (*abort || global_timer_ns() - t0 > kWaitLimitNs)) {
         flag_timeout(p.errors, kTimeoutProducer);
         *abort = 1;
+        ok = 0;
         break;
       }
     }
   }
-  __syncthreads();
-  return *abort == 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  return ok != 0;
 }
 
 // Barrier among the epilogue warps only, returning pred ORed (AND = false:
@@ -345,8 +376,6 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
     pdl_launch_dependents();
     pdl_wait();
   }
-  // the decode step's insert and query quantisation, then the grid barrier
-  if (STEP) decode_step_prologue<H, NEXT_N>(p, abort);
   // The item loader's operands (warp 5), read into registers before they are
   // staged, all loads of a lane in flight together:
   //   B operand: row r = j*H + h of the sequence's query heads, 64 bytes,
@@ -383,7 +412,10 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   // The loader's first item is this CTA's own index: its operands are read
   // now, for all of the item's tiles, while the block fills the context-length
   // cache that decides how many of them are used.
-  const bool preloaded = warp == kLoaderWarp && (int64_t)blockIdx.x < (int64_t)p.B * p.chunks;
+  // (not in the decode step: there the operands exist once the item's
+  // sequence has been prepared)
+  const bool preloaded =
+      !STEP && warp == kLoaderWarp && (int64_t)blockIdx.x < (int64_t)p.B * p.chunks;
   if (preloaded)
     load_operands((int32_t)(blockIdx.x % p.B),
                   (int64_t)(blockIdx.x / p.B) * p.tiles_per_cta * kTileKeys, p.tiles_per_cta);
@@ -400,6 +432,21 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   if (warp == kLoaderWarp) {
     // ---------------------------------------------------------- item loader
     constexpr uint32_t kAll = 0xFFFFFFFFu;
+    if (STEP) {
+      // the decode step's preparation chunks, claimed until none is left
+      constexpr uint32_t kCh = (uint32_t)step_chunks<H, NEXT_N>();
+      const uint32_t total = (uint32_t)p.B * kCh;
+      while (true) {
+        uint32_t c = 0;
+        if (lane == 0) c = claim_item(p.prep_counter, p.item_gen, p.errors);
+        c = __shfl_sync(kAll, c, 0);
+        if (c >= total) break;
+        step_prepare_chunk<H, NEXT_N>(p, (int32_t)(c / kCh), (int)(c % kCh), lane);
+        __threadfence();  // the chunk's stores before the count that publishes them
+        __syncwarp();
+        if (lane == 0) (void)claim_item(p.seq_state + c / kCh, p.item_gen, p.errors);
+      }
+    }
     int n = 0;
     int64_t w = (int64_t)blockIdx.x - (int64_t)gridDim.x;
     bool first = true;
@@ -424,6 +471,10 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
         it = paged_item(p, w, sCl, lane == 0);
         if (it.n_tiles > 0 || pass_empty) break;
       }
+      // the decode step: the sequence's query heads and new keys first (an
+      // item stream that gives up there ends here for every role)
+      if (STEP && it.n_tiles > 0 && !step_wait_sequence<H, NEXT_N>(p, it.b, lane, abort))
+        it.n_tiles = -1;
       if (it.n_tiles > 0 && !(preloaded && w == (int64_t)blockIdx.x))
         load_operands(it.b, it.k0, it.n_tiles);
       const int qb = n & 1;

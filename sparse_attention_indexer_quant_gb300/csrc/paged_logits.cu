@@ -10,8 +10,6 @@
 // to the logits row (-inf past the window when the rows are clean).
 #include <math.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "launch.h"
 #include "paged_core.cuh"
@@ -61,38 +59,14 @@ struct UnfusedEpilogue {
   }
 };
 
-// STEP: the decode step's scoring pass, which first inserts the step's new
-// keys and quantises its query heads (decode_step_prologue), launched as a
-// cooperative grid.
+// STEP: the decode step's scoring pass, which prepares each sequence (its
+// query heads quantised, its new keys inserted) before scoring its items
+// (step_prepare_sequence).
 template <int H, int NEXT_N, bool STEP>
 __global__ void __launch_bounds__(paged_threads(H * NEXT_N), paged_ctas_per_sm(H * NEXT_N))
     paged_logits_kernel(const PagedArgs p) {
   paged_persistent_run<H, NEXT_N, UnfusedEpilogue<H, NEXT_N>, STEP>(
       p, p.kcache, p.item_counter != nullptr, p.clean != 0, p.item_counter);
-}
-
-// CTAs of the kernel resident per SM by the occupancy calculator, once per
-// device: the cooperative launch of the decode step is refused beyond it.
-template <int H, int NEXT_N, bool STEP>
-int resident_ctas_per_sm(size_t smem, int planned) {
-  auto kern = paged_logits_kernel<H, NEXT_N, STEP>;  // one cache per kernel
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static int cache[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return planned;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, paged_threads(H * NEXT_N), smem) !=
-            cudaSuccess ||
-        n <= 0) {
-      (void)cudaGetLastError();
-      n = 1;
-    }
-    cache[dev] = n < planned ? n : planned;
-  }
-  return cache[dev];
 }
 
 template <int H, int NEXT_N, bool STEP>
@@ -106,15 +80,8 @@ cudaError_t launch_one(const PagedArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  if (!STEP)
-    return launch_dependent(kern, dim3((unsigned)a.grid), dim3(paged_threads(H * NEXT_N)), smem,
-                            stream, a);
-  // the cooperative launch: no more CTAs than the runtime counts as resident
-  const int per_sm = resident_ctas_per_sm<H, NEXT_N, STEP>(smem, paged_ctas_per_sm(H * NEXT_N));
-  const int64_t cap = (int64_t)(a.sms > 0 ? a.sms : 1) * per_sm;
-  const unsigned grid = (unsigned)(a.grid < cap ? a.grid : cap);
-  return launch_dependent_coop(kern, dim3(grid), dim3(paged_threads(H * NEXT_N)), smem, stream,
-                               a);
+  return launch_dependent(kern, dim3((unsigned)a.grid), dim3(paged_threads(H * NEXT_N)), smem,
+                          stream, a);
 }
 
 template <bool STEP>
@@ -129,7 +96,7 @@ cudaError_t launch_shape(int H, int next_n, const PagedArgs& a, cudaStream_t str
 }  // namespace
 
 cudaError_t launch_paged_logits(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
-  return a.grid_bar != nullptr ? launch_shape<true>(H, next_n, a, stream)
+  return a.seq_state != nullptr ? launch_shape<true>(H, next_n, a, stream)
                                : launch_shape<false>(H, next_n, a, stream);
 }
 

@@ -27,33 +27,36 @@ namespace idx {
 namespace {
 
 struct TopkWs {
-  unsigned long long* items;  // work-item counter of the scoring pass
-  unsigned long long* bar;    // the decode step's grid-barrier arrivals
+  unsigned long long* items;  // work-item counter of the scoring pass, then the
+                              // decode step's preparation-chunk counter
   float* logits;              // [rows][ldw]
   int64_t ldw;
   uint8_t* q_vals;            // decode step: quantised query heads [rows * H][64]
   uint8_t* q_scales;          //              and their scales [rows * H][4]
+  unsigned long long* seq_state;  // decode step: per-sequence preparation state [B]
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
 
 // H = 0: the fused call's workspace; H > 0: the decode step's, which also
-// holds the step's quantised query heads after the logits.
+// holds the step's quantised query heads and one state word per sequence
+// after the logits (rows = B * next_n).
 __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t max_blocks,
-                                            size_t* total, int32_t H = 0) {
+                                            size_t* total, int32_t H = 0, int32_t B = 0) {
   const int64_t ldw = (int64_t)max_blocks * kPage;
   const size_t o_lg = 256;
   const size_t o_qv = o_lg + ws_align((size_t)rows * ldw * 4);
   const size_t o_qs = o_qv + ws_align((size_t)rows * H * kValBytes);
+  const size_t o_st = o_qs + ws_align((size_t)rows * H * kScaleBytes);
   uint8_t* p = static_cast<uint8_t*>(base);
   TopkWs w;
   w.items = reinterpret_cast<unsigned long long*>(p);
-  w.bar = w.items + 1;
   w.logits = reinterpret_cast<float*>(p + o_lg);
   w.ldw = ldw;
   w.q_vals = H > 0 ? p + o_qv : nullptr;
   w.q_scales = H > 0 ? p + o_qs : nullptr;
-  if (total) *total = H > 0 ? o_qs + ws_align((size_t)rows * H * kScaleBytes) : o_qv;
+  w.seq_state = H > 0 ? reinterpret_cast<unsigned long long*>(p + o_st) : nullptr;
+  if (total) *total = H > 0 ? o_st + ws_align((size_t)B * 8) : o_qv;
   return w;
 }
 
@@ -75,12 +78,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const Page
   int64_t len = L - next_n + j + 1;
   len = len < 0 ? 0 : len;
   pdl_wait();  // the scoring pass's logits
-  // the work-item counter (and the decode step's barrier count) are done
-  // with: clear them, so that a replay of this call with the same generation
-  // (a CUDA graph) finds no claims or arrivals of its own
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    ws.items[0] = 0ull;
-    ws.items[1] = 0ull;
+  // the work-item counter (and the decode step's chunk counter and counts)
+  // are done with: reset them to this call's generation with no claims, so
+  // that a replay of this call (a CUDA graph, same generation) starts from
+  // zero without installing its generation first (a call with another
+  // generation still finds them stale and installs its own)
+  if (blockIdx.x == 0) {
+    const unsigned long long fresh = p.item_gen << kItemBits;
+    if (threadIdx.x < 2) ws.items[threadIdx.x] = fresh;  // scoring items, step chunks
+    if (p.seq_state != nullptr)
+      for (int i = threadIdx.x; i < p.B; i += kSelThreads) p.seq_state[i] = fresh;
   }
   // the workspace rows are 256-byte aligned
   cluster_select_row(sm, ws.logits + r * ws.ldw, len, (uint32_t)p.topk, p.out_idx + r * p.topk,
@@ -111,19 +118,20 @@ size_t paged_step_workspace_bytes(int32_t B, int32_t next_n, int32_t H, int32_t 
   (void)k;
   if (B <= 0 || (next_n != 1 && next_n != 2) || max_blocks <= 0 || H <= 0) return 0;
   size_t total = 0;
-  ws_layout(nullptr, (int64_t)B * next_n, max_blocks, &total, H);
+  ws_layout(nullptr, (int64_t)B * next_n, max_blocks, &total, H, B);
   return total;
 }
 
 cudaError_t launch_paged_decode_step(int H, int next_n, const PagedArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.B * next_n;
-  const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr, H);
+  const TopkWs ws = ws_layout(a.workspace, rows, a.max_blocks, nullptr, H, a.B);
   PagedArgs s = a;
   s.q_vals = ws.q_vals;
   s.q_scales = ws.q_scales;
   s.q_vals_w = ws.q_vals;
   s.q_scales_w = ws.q_scales;
-  s.grid_bar = ws.bar;
+  s.seq_state = ws.seq_state;
+  s.prep_counter = ws.items + 1;
   return launch_paged_logits_topk(H, next_n, s, stream);
 }
 

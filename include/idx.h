@@ -327,8 +327,8 @@ IDX_API idx_status idx_paged_logits_topk_noalloc(
  *                256-byte aligned, no initialisation, not shared by calls that
  *                overlap on the GPU.  Besides the fused call's contents it
  *                holds the quantised query heads, a chunk counter and one
- *                count per sequence (generation-tagged, cleared by the
- *                select).
+ *                count per sequence (generation-tagged; the select resets
+ *                them to the call's generation with no claims).
  *   The scoring launch does the step's quantisation and insert first, in
  *   small chunks that its CTAs claim from a counter in the workspace; a CTA
  *   waits for a sequence's chunks to be done before it reads any of the

@@ -90,3 +90,37 @@ def test_noalloc_refuses_batches_above_its_scratch(idx):
     out = torch.empty((64, 2048), dtype=torch.int32, device="cuda")
     big.block_table = bt
     assert _call_noalloc(idx, d, big, 2048, out) == 1
+
+
+def test_noalloc_through_the_binding(idx, oracle):
+    """The Python binding of the entry, on a batch at both head counts' MMA
+    widths of the decode core (H = 32, next_n = 1 and 2), with the refusal
+    raised as an IdxError carrying the library's detail."""
+    for seed, next_n in ((910, 1), (911, 2)):
+        p = wl.make_decode("t", seed, [64, 2048, 2049, 7000], 32, next_n)
+        cache = dev(wl.poisoned_cache(p.num_blocks))
+        idx.quant_insert(dev_bf16(p.k), dev(p.slots), cache)
+        qv, qs = idx.quant_q(dev_bf16(p.q))
+        errs = idx.new_errors()
+        got = idx.paged_logits_topk_noalloc(qv, qs, dev(p.weights), cache, dev(p.block_table),
+                                            dev(p.context_lens), next_n, 32, 2048, errors=errs)
+        torch.cuda.synchronize()
+        assert errs.cpu().tolist() == [0, 0]
+        ocache = wl.poisoned_cache(p.num_blocks)
+        oracle.quant_insert(p.k, p.slots, ocache)
+        oqv, oqs = oracle.quant_q(p.q)
+        ol, om = oracle.paged_mqa_logits(oqv, oqs, p.B, next_n, 32, ocache, p.block_table,
+                                         p.context_lens, p.weights, p.block_table.shape[1] * 64)
+        st, en = p.row_windows()
+        g = got.cpu().numpy()
+        for r in range(p.rows):
+            n = int(en[r])
+            check_topk(g[r], ol[r, :n], om[r, :n], n, 2048, f"next_n {next_n} row {r}")
+    p = wl.make_decode("t", 912, [100], 32, 1, max_blocks=4096)
+    bt = dev(np.tile(p.block_table, (64, 1)))
+    cache = dev(wl.poisoned_cache(p.num_blocks))
+    qv, qs = idx.quant_q(dev_bf16(np.tile(p.q, (64, 1, 1))))
+    with pytest.raises(idx.IdxError) as e:
+        idx.paged_logits_topk_noalloc(qv, qs, dev(np.tile(p.weights, (64, 1))), cache, bt,
+                                      dev(np.tile(p.context_lens, 64)), 1, 32, 2048)
+    assert e.value.status == 1 and e.value.detail  # invalid argument, with the reason

@@ -39,6 +39,7 @@ METRIC = "decode K-tokens scored/s + HBM GB/s (paged MXFP4 MQA logits + top-k)"
 UNIT = "key-tokens/s"
 TOPK = 2048
 L2_FLUSH_BYTES = 256 << 20   # 2x the 129 MB L2
+SMS_GB300 = 152
 # sources of the fused decode entry (scoring + select launches); the committed
 # traffic figure is only used while their digest matches
 FUSED_SOURCES = ["paged_topk.cu", "paged_logits.cu", "paged_core.cuh", "select_row.cuh",
@@ -369,6 +370,7 @@ def run_ours(args, rank, world, local_rank):
         also.update(insert_entries(idx, dev, flush_l2, stream))
         also.update(next_entries(idx, dev, flush_l2, stream))
         also.update(step_entries(idx, dev, flush_l2, stream))
+        also.update(mixed_prefill_entry(idx, dev, flush_l2, stream))
         for other in ("long_decode", "mixed_decode", "pr_ref"):
             if other != args.workload:
                 also[other] = decode_workload_entry(other, idx, dev, flush_l2, stream)
@@ -746,9 +748,18 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
                            "ms": pre_ms, "tflops": tf, "peak_tflops": peak_tf,
                            "peak_source": peak_src, "frac": tf / peak_tf,
                            "store_gbs": pairs * 4 / (pre_ms * 1e-3) / 1e9,
-                           "valid_pairs": pairs},
+                           "store_frac_of_hbm": pairs * 4 / (pre_ms * 1e-3) / 1e9 / hbm,
+                           "valid_pairs": pairs,
+                           # the CUDA-core epilogue: one max and one multiply-add per
+                           # accumulator value (pairs x H); at the ALU pipe's rate for the
+                           # max, 64 values per cycle per SM at the 2070 MHz SM clock
+                           "epilogue_values": pairs * p.H,
+                           "epilogue_floor_ms": pairs * p.H / (64.0 * SMS_GB300 * 2.07e9) * 1e3},
         "prefill_topk": {"workload": "32768 causal rows, k=2048", "ms": topk_ms,
-                         "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9},
+                         "read_gbs": pairs * 4 / (topk_ms * 1e-3) / 1e9,
+                         # the logits read once and k indices written per row
+                         "frac_of_hbm": (pairs * 4 + p.T * TOPK * 4) / (topk_ms * 1e-3) / 1e9
+                                        / hbm},
         "prefill_cpu_baseline": pre_cpu,
         "prefill_logits_topk_fused": {
             "workload": "causal 32768 x 32768, H=32, k=2048, no logits tensor",
@@ -756,6 +767,57 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
             "tflops": tf * pre_ms / fused_ms},
     })
     return res
+
+
+def mixed_prefill_entry(idx, dev, flush_l2, stream, reps=5):
+    """The chunked-prefill half of the mixed batch (8 sequences, prefixes
+    U[0, 65536], 8192 new tokens each): the gather of every sequence's cached
+    keys, then per sequence the causal logits over its gathered keys and the
+    top-k of its rows, as a serving step issues them; L2 flushed once before
+    each repetition."""
+    import torch
+    from sparse_attention_indexer_quant_gb300 import workloads as wl
+    p = wl.mixed_prefill_part()
+    cache = torch.from_numpy(wl.poisoned_cache(p.num_blocks)).to(dev)
+    idx.quant_insert(bf16_tensor(p.k, dev), torch.from_numpy(p.slots).to(dev), cache)
+    lens = (p.prefix_lens.astype(np.int64) + p.new_lens).astype(np.int32)
+    offs = p.tok_offsets[:-1].astype(np.int64)
+    S = int(p.tok_offsets[-1])
+    bt, ln, of = (torch.from_numpy(x).to(dev) for x in (p.block_table, lens, offs))
+    kv, ks = idx.gather_k(cache, bt, ln, of, S)
+    qv, qs = idx.quant_q(bf16_tensor(p.q, dev))
+    w = torch.from_numpy(p.weights).to(dev)
+    q_off = np.concatenate([[0], np.cumsum(p.new_lens)]).astype(np.int64)
+    H = p.H
+    Tmax, Lmax = int(p.new_lens.max()), int(lens.max())
+    logits = torch.empty((Tmax, Lmax), dtype=torch.float32, device=dev)
+    out = torch.empty((Tmax, TOPK), dtype=torch.int32, device=dev)
+    calls, pairs = [], 0
+    for b in range(p.B):
+        L, P, T = int(lens[b]), int(p.prefix_lens[b]), int(p.new_lens[b])
+        st = torch.zeros(T, dtype=torch.int32, device=dev)
+        en = torch.from_numpy((P + np.arange(T) + 1).astype(np.int32)).to(dev)
+        qa, qb = int(q_off[b]), int(q_off[b + 1])
+        pairs += int(T * P + T * (T + 1) // 2)
+        calls.append((qv[qa * H:qb * H], qs[qa * H:qb * H], w[qa:qb], kv[offs[b]:offs[b] + L],
+                      ks[offs[b]:offs[b] + L], st, en, T, L))
+
+    def step():
+        idx.gather_k(cache, bt, ln, of, S)
+        for qvb, qsb, wb, kvb, ksb, st, en, T, L in calls:
+            lg = logits[:T].view(-1)[:T * L].view(T, L)
+            idx.mqa_logits(qvb, qsb, wb, kvb, ksb, st, en, H, out=lg)
+            idx.topk_rows(lg, en, TOPK, out=out[:T])
+
+    ms = time_op(step, flush_l2, stream, reps)
+    flops = 2.0 * H * 128 * pairs
+    peak_tf, peak_src = mxf4_peak_tflops()
+    return {"mixed_prefill": {
+        "workload": "the mixed batch's 8 chunked prefills (prefix U[0, 65536] + 8192 new, "
+                    "H=32): gather, then per sequence logits and top-k",
+        "ms": ms, "valid_pairs": pairs, "tflops": flops / (ms * 1e-3) / 1e12,
+        "frac_of_mxf4_peak": flops / (ms * 1e-3) / 1e12 / peak_tf, "peak_source": peak_src,
+        "note": "the step's time includes the top-k of every row and the gather"}}
 
 
 def host_cpu_info():

@@ -618,8 +618,9 @@ def step_entries(idx, dev, flush_l2, stream, reps=50):
             "workload": WORKLOADS[name][1],
             "two_launch_step_us": ms2 * 1e3, "four_launch_step_us": ms4 * 1e3,
             "timing": f"median of {reps} CUDA-graph replays, L2 flushed before each",
-            "note": "the two-launch step's scoring launch is cooperative, so the runtime caps it "
-                    "at one CTA per SM"}
+            "note": "the two-launch step's scoring launch first quantises the query heads and "
+                    "inserts the new keys in chunks its CTAs claim; a CTA waits for a "
+                    "sequence's chunks before reading its keys"}
         del cache
     return res
 

@@ -391,7 +391,8 @@ __device__ __forceinline__ void paged_persistent_run(const PagedArgs& p, const u
   int32_t id_r[4];
   auto load_operands = [&](int32_t b, int64_t k0, int32_t n_tiles) {
     const uint4* qv = reinterpret_cast<const uint4*>(p.q_vals + (int64_t)b * NH * kValBytes);
-    // (in the decode step this kernel's prologue wrote them: loads through L2)
+    // (in the decode step this launch's preparation chunks wrote them: loads
+    // through L2)
 #pragma unroll
     for (int u = 0; u < kQv; ++u) qv_r[u] = STEP ? __ldcg(qv + lane + 32 * u) : __ldg(qv + lane + 32 * u);
     const uint32_t* qs = reinterpret_cast<const uint32_t*>(p.q_scales) + (int64_t)b * NH;

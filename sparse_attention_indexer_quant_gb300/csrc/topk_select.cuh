@@ -92,30 +92,46 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanScratch
 
 // Finds the bin b of hist[0, nbins) with count(bins > b) < need <= count(bins >= b)
 // and stores b and count(bins > b) in sc.bin / sc.above.  Requires
-// 1 <= need <= total count.
+// 1 <= need <= total count.  Warp w sums the w-th segment of bins from the
+// top (its lanes on consecutive bins, so the reads are free of bank
+// conflicts); the warp whose segment holds the need-th element then walks
+// it from the top, 32 bins a step, with a warp scan.
 __device__ __forceinline__ void find_threshold_bin(const uint32_t* hist, int nbins, uint32_t need,
                                                    ScanScratch& sc) {
-  const int nt = blockDim.x;
-  const int per = (nbins + nt - 1) / nt;
-  const int hi = nbins - 1 - (int)threadIdx.x * per;   // this thread's bins: (hi - per, hi]
-  uint32_t local = 0;
-  for (int q = 0; q < per; ++q) {
-    const int bin = hi - q;
-    if (bin >= 0) local += hist[bin];
-  }
-  const uint32_t excl = block_exclusive_scan(local, sc);
-  if (excl < need && need <= excl + local) {
-    uint32_t run = excl;
-    for (int q = 0; q < per; ++q) {
-      const int bin = hi - q;
-      if (bin < 0) break;
-      const uint32_t h = hist[bin];
-      if (run + h >= need) {
-        sc.bin = (uint32_t)bin;
-        sc.above = run;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (int)(blockDim.x >> 5);
+  const int seg = (nbins + nw - 1) / nw;
+  const int hi = nbins - warp * seg;   // the warp's bins: [lo, hi)
+  const int lo = hi - seg > 0 ? hi - seg : 0;
+  uint32_t sum = 0;
+  for (int i = lo + lane; i < hi; i += 32) sum += hist[i];
+  sum = __reduce_add_sync(0xFFFFFFFFu, sum);
+  if (lane == 0) sc.warp_sums[warp] = sum;
+  __syncthreads();
+  uint32_t above = 0;  // elements in the segments above this warp's
+  for (int q = 0; q < warp; ++q) above += sc.warp_sums[q];
+  if (above < need && need <= above + sum) {
+    uint32_t run = above;
+    for (int top = hi; top > lo; top -= 32) {
+      const int bin = top - 1 - lane;  // lane 0 on the row's highest bin
+      const uint32_t h = bin >= lo ? hist[bin] : 0u;
+      uint32_t incl = h;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, run + incl >= need);
+      if (hit != 0u) {
+        const int l = __ffs(hit) - 1;
+        const uint32_t before = __shfl_sync(0xFFFFFFFFu, incl - h, l);
+        if (lane == 0) {
+          sc.bin = (uint32_t)(top - 1 - l);
+          sc.above = run + before;
+        }
         break;
       }
-      run += h;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
   __syncthreads();

@@ -127,6 +127,13 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
     for (int64_t base = 0; base < len; base += kRound) {
       float4 v[kVec];
       load_round(base, v);
+      // the next round's lines start on their way to L2 while this round's
+      // keys are counted (no registers held for them)
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) {
+        const int64_t i1 = base + kRound + 4 * ((int64_t)u * kRowThreads + threadIdx.x);
+        if (i1 < len) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + i1));
+      }
 #pragma unroll
       for (int u = 0; u < kVec; ++u) {
         const int64_t i0 = base + 4 * ((int64_t)u * kRowThreads + threadIdx.x);

@@ -33,9 +33,9 @@
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates no device memory and never synchronises; work is enqueued on
  *     `stream` (NULL = the legacy default stream) and the call returns at once.
- *     So every call can be captured in a CUDA graph; a replay reads its
- *     buffers afresh (the fused call's work-item counter starts over on every
- *     replay).
+ *     So every call other than idx_paged_logits_topk_noalloc can be captured
+ *     in a CUDA graph; a replay reads its buffers afresh (the fused call's
+ *     work-item counter starts over on every replay).
  *   - Argument and device errors are returned synchronously, before anything is
  *     enqueued.  IDX_ERR_CUDA reports a launch failure (the CUDA error string
  *     is available from idx_last_error_detail()).
@@ -290,8 +290,8 @@ IDX_API idx_status idx_paged_logits_topk(const uint8_t* q_vals, const uint8_t* q
  *   The scratch is a 32 MiB array inside the library: every GPU that loads the
  *   library reserves it until the process exits.  Its device address is looked
  *   up on the first call in each CUDA context (the calling thread's current
- *   one), so make that first call before any stream capture, and again after
- *   a device reset (which ends the context).
+ *   one) and kept for later calls in that context; a device reset ends the
+ *   context, and the next call looks the address up again.
  *   A batch whose idx_paged_logits_topk_workspace_bytes exceeds 32 MiB is
  *   rejected with IDX_ERR_INVALID_ARG (the reason is in
  *   idx_last_error_detail()); use idx_paged_logits_topk with a caller

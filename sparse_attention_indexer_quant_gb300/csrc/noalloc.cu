@@ -14,7 +14,7 @@
 //     library and stays reserved until the process exits;
 //   - its device address is looked up on the first call in each CUDA context
 //     (the current one of the calling thread) and kept for later calls in
-//     that context; make that first call before any stream capture;
+//     that context;
 //   - all calls share the one array, so calls that overlap on the GPU (on
 //     different streams without ordering) race and give wrong results;
 //   - nothing has to be cleared between calls: the work-item counter at the

@@ -366,7 +366,8 @@ def run_ours(args, rank, world, local_rank):
     also = None
     if rank == 0 and not args.no_also:
         also = secondary_measurements(idx, dev, flush_l2, stream,
-                                      decode=(p, cache, qv, qs, w, bt, cl))
+                                      decode=(p, cache, qv, qs, w, bt, cl),
+                                      decode_desc=WORKLOADS[args.workload][1])
         also.update(insert_entries(idx, dev, flush_l2, stream))
         also.update(next_entries(idx, dev, flush_l2, stream))
         also.update(step_entries(idx, dev, flush_l2, stream))
@@ -665,11 +666,12 @@ def next_entries(idx, dev, flush_l2, stream, reps=10):
     return res
 
 
-def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
+def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None, decode_desc=""):
     """The other steps of the path, each timed alone with a flushed L2: insert,
     q-quant, gather, prefill logits and top-k on the 32K-token causal prefill
-    (one sequence, H = 32); with `decode` (the batched decode state), the
-    unfused paged logits and the top-k of its rows."""
+    (one sequence, H = 32); with `decode` (the timed decode workload's state,
+    described by `decode_desc`), the unfused paged logits and the top-k of its
+    rows."""
     import torch
     from sparse_attention_indexer_quant_gb300 import workloads as wl
     hbm, _ = peaks()
@@ -687,11 +689,11 @@ def secondary_measurements(idx, dev, flush_l2, stream, reps=10, decode=None):
         dout = torch.empty((dp.rows, TOPK), dtype=torch.int32, device=dev)
         dk_ms = time_op(lambda: idx.topk_rows(lg, en_d, TOPK, out=dout), flush_l2, stream, reps)
         res["paged_logits_unfused"] = {
-            "workload": "batched decode, logits rows written to HBM (unclean)", "ms": pl_ms,
+            "workload": f"{decode_desc}: logits rows written to HBM (unclean)", "ms": pl_ms,
             "gbs": pl_bytes / (pl_ms * 1e-3) / 1e9,
             "frac_of_hbm": pl_bytes / (pl_ms * 1e-3) / 1e9 / hbm}
         res["decode_topk_rows"] = {
-            "workload": "the batched decode's 64 logits rows, k=2048", "ms": dk_ms,
+            "workload": f"the decode's {dp.rows} logits rows, k=2048", "ms": dk_ms,
             "read_gbs": (4 * n_logits + dp.rows * TOPK * 4) / (dk_ms * 1e-3) / 1e9}
         del lg
     p = wl.prefill()

@@ -45,14 +45,15 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 // Occupancy plan per N = next_n * H.  Streaming random pages reaches HBM rate
 // only with about 200 KB of copies in flight per SM (loaded latency is several
 // microseconds), so each shape gets as many stage buffers as its CTAs-per-SM
-// allow: N = 32 three CTAs of 7 stages, N = 64 two of 10, N = 128 (whose
-// epilogue needs the registers of a whole SM) one of 20.
-__host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 32 ? 3 : nh == 64 ? 2 : 1; }
-__host__ __device__ constexpr int paged_stages(int nh) { return nh == 32 ? 7 : nh == 64 ? 10 : 20; }
+// allow: N = 32 three CTAs of 7 stages, N = 64 two of 10, N = 128 two of 10
+// (with one accumulator each: the two CTAs' MMAs and epilogues interleave on
+// the SM, which streams faster than one CTA of 20 stages with three).
+__host__ __device__ constexpr int paged_ctas_per_sm(int nh) { return nh == 32 ? 3 : 2; }
+__host__ __device__ constexpr int paged_stages(int nh) { return nh == 32 ? 7 : 10; }
 // Epilogue warps: four (one per TMEM lane quarter) take all N columns of their
-// keys; at N = 128 (one CTA per SM) eight, a pair per lane quarter, each
-// taking one query's 64 heads, so that each SM sub-partition has two warps
-// forming sums.  Then the MMA warp, the item loader and two copy producers.
+// keys; at N = 128 eight, a pair per lane quarter, each taking one query's 64
+// heads, so that each SM sub-partition has four warps forming sums.  Then the
+// MMA warp, the item loader and two copy producers.
 __host__ __device__ constexpr int paged_epi_warps(int nh) { return nh == 128 ? 8 : 4; }
 __host__ __device__ constexpr int paged_threads(int nh) { return 32 * (paged_epi_warps(nh) + 4); }
 
@@ -69,10 +70,11 @@ template <int NH>
 struct PagedLayout {
   static constexpr int kStages = paged_stages(NH);
   // accumulators: as many as fit the TMEM share of a CTA (512 columns per SM:
-  // 128 for each of three N = 32 CTAs, 256 for each of two N = 64 CTAs, all
-  // for one N = 128 CTA); three in every case, so that three tiles' MMAs can
-  // be in flight while the epilogue reads a fourth's
-  static constexpr int kAccBufs = 3;
+  // 128 for each of three N = 32 CTAs, 256 for each of two N = 64 or N = 128
+  // CTAs): three at N = 32 and 64, so that three tiles' MMAs can be in flight
+  // while the epilogue reads a fourth's; one at N = 128, where the SM's other
+  // CTA covers the wait
+  static constexpr int kAccBufs = NH == 128 ? 1 : 3;
   static constexpr uint32_t kSfbCol = kAccBufs * NH;        // 2 x 4 columns
   static constexpr uint32_t kSfaCol = kSfbCol + 8;          // 4 columns per accumulator
   static constexpr uint32_t kTmemCols = tmem_cols_for(kSfaCol + 4 * kAccBufs);

@@ -7,7 +7,12 @@
 //               from a generation-tagged counter and writing each row's valid
 //               logits to a row-major scratch that stays in L2 for these sizes;
 //   2. select   one thread-block cluster of P CTAs per row running
-//               cluster_select_row (select_row.cuh) over the row's logits.
+//               cluster_select_row (select_row.cuh) over the row's logits;
+//               where one CTA per row is all that fits in one wave (more
+//               rows than half the SMs), two-CTA clusters in two waves
+//               instead, each cluster taking the sequences in order of
+//               decreasing length, so that the longest rows (the slowest
+//               selects) are in the first wave.
 // Both are dependent launches.  The scoring pass lets the select launch start
 // only once every earlier kernel is done, so the select reads the call's
 // inputs before waiting for the logits.
@@ -60,15 +65,40 @@ __host__ __device__ inline TopkWs ws_layout(void* base, int64_t rows, int32_t ma
   return w;
 }
 
-// One cluster of `parts` CTAs per query row (b, j) of the decode batch.
+// One cluster of `parts` CTAs per query row (b, j) of the decode batch; with
+// `by_length` cluster c takes query j = c % next_n of the (c / next_n)-th
+// longest sequence (equal lengths: lower index first; needs B <= kCoarseBins).
 __global__ void __launch_bounds__(kSelThreads, 1) paged_select_kernel(const PagedArgs p, int next_n,
-                                                                      int parts) {
+                                                                      int parts, int by_length) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int64_t rows = (int64_t)p.B * next_n;
   const TopkWs ws = ws_layout(p.workspace, rows, p.max_blocks, nullptr);
-  const int64_t r = blockIdx.x / parts;
-  const int b = (int)(r / next_n), j = (int)(r % next_n);
+  int64_t r = blockIdx.x / parts;
+  int b = (int)(r / next_n);
+  const int j = (int)(r % next_n);
+  if (by_length) {
+    // the context lengths (clamped to the block table) in the histogram's
+    // space, which the select clears only after this; each thread ranks its
+    // sequences against all others, and the one of rank b is the cluster's
+    const int64_t cap = (int64_t)p.max_blocks * kPage;
+    int32_t* lens = reinterpret_cast<int32_t*>(sm.bins);
+    __shared__ int picked;
+    for (int i = threadIdx.x; i < p.B; i += kSelThreads) {
+      const int64_t v = __ldg(p.context_lens + i);
+      lens[i] = (int32_t)(v < 0 ? 0 : (v > cap ? cap : v));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.B; i += kSelThreads) {
+      const int32_t li = lens[i];
+      int rank = 0;
+      for (int q = 0; q < p.B; ++q) rank += (lens[q] > li || (lens[q] == li && q < i)) ? 1 : 0;
+      if (rank == b) picked = i;  // ranks are distinct: exactly one thread writes
+    }
+    __syncthreads();
+    b = picked;
+    r = (int64_t)b * next_n + j;
+  }
   // an input of the call, read before the wait: this launch can only have
   // started after the scoring pass's wait, i.e. after every kernel issued
   // before the call completed
@@ -157,10 +187,19 @@ cudaError_t launch_paged_logits_topk(int H, int next_n, const PagedArgs& a, cuda
   s.wait_first = 1;
   e = launch_paged_logits(H, next_n, s, stream);
   if (e != cudaSuccess) return e;
-  const int parts = select_parts(paged_select_kernel, 0, rows, ws.ldw, a.sms > 0 ? a.sms : 1, smem);
+  const int sms = a.sms > 0 ? a.sms : 1;
+  int parts = select_parts(paged_select_kernel, 0, rows, ws.ldw, sms, smem);
+  // one CTA per row fits one wave but two do not: two-CTA clusters in two
+  // waves, longest rows first (128 rows of 1K - 128K keys: 123 us for the
+  // call against 130 with one CTA per row, whose longest selects took ~30 us)
+  int by_length = 0;
+  if (parts == 1 && rows <= (int64_t)sms && ws.ldw / 2 >= kMinSlice && a.B <= kCoarseBins) {
+    parts = 2;
+    by_length = 1;
+  }
   return launch_dependent_cluster(paged_select_kernel, dim3((unsigned)(rows * parts)),
                                   dim3(kSelThreads), smem, stream, (unsigned)parts, a, next_n,
-                                  parts);
+                                  parts, by_length);
 }
 
 }  // namespace idx

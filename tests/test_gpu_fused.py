@@ -194,3 +194,24 @@ def test_fused_more_sequences_than_ctas(idx, oracle):
     g = run_fused(idx, p, 2048)
     for b, (ol, om, L) in oracle_rows(oracle, p, [0, 1, 3, 200, 455, 456, 457, 498, 499]).items():
         check_topk(g[b], ol[0, :L], om[0, :L], L, 2048, f"seq {b}")
+
+
+@pytest.mark.parametrize("B,next_n", [(100, 1), (48, 2)])
+def test_fused_two_select_waves_longest_first(idx, oracle, B, next_n):
+    """More query rows than half the SMs: the select runs two-CTA clusters in
+    two waves, each cluster taking the sequences in order of decreasing length.
+    Every row is checked, with equal lengths (the order breaks ties by index),
+    empty rows and rows at k."""
+    rng = np.random.default_rng(4242 + B)
+    lens = [int(x) for x in rng.integers(0, 6000, size=B)]
+    for b, L in [(0, 3000), (1, 3000), (2, 3000), (3, 3000), (4, 0), (5, 0), (6, 2048),
+                 (7, 2050), (8, 9000), (9, 9000), (B - 1, 3000)]:
+        lens[b] = L
+    p = wl.make_decode("two_waves", 4242 + B, lens, 32, next_n)
+    assert p.rows > 76 and p.block_table.shape[1] * 64 >= 8192
+    g = run_fused(idx, p, 2048)
+    for b, (ol, om, L) in oracle_rows(oracle, p, range(B)).items():
+        for j in range(next_n):
+            n = max(L - next_n + j + 1, 0)
+            check_topk(g[b * next_n + j], ol[j, :n], om[j, :n], n, 2048,
+                       f"seq {b} (L={L}) row {j}")

@@ -29,7 +29,7 @@
 // value and position, with one shared-memory slot claim per warp) iff its key
 // is >= tau.  Every logit >= tau is therefore in the list and at least k of
 // them are, so the row's k largest are in the list; tau only grows (one warp
-// per query pair recomputes it every few tiles from a possibly stale, never
+// per query pair recomputes it every kTkEvery tiles from a possibly stale, never
 // over-counted histogram).  A second kernel selects the exact top-k of each
 // list (topk.cu).
 #include <math.h>
@@ -48,7 +48,8 @@ constexpr int kEpiWarps = 16;
 
 constexpr int kTkBins = 1024;      // candidate histogram: top 10 key bits
 constexpr int kTkShift = 22;
-constexpr int kTkEvery = 8;        // tiles between threshold updates (per query pair)
+constexpr int kTkEvery = 32;       // tiles between threshold updates (per query pair; an
+                                   // update holds up its warp, and so the next tile)
 
 // shared memory of the candidate state, per query of the group
 struct TopkState {
@@ -338,16 +339,13 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
             uint32_t base = 0;
             if (lane == 0) base = atomicAdd(&ts.cnt, (uint32_t)__popc(ballot));
             base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            // the histogram: one shared atomic per distinct bin of the warp
-            // (a warp's logits share a few bins; per-lane atomics would
-            // serialise on one address)
-            const uint32_t bin = kk >> kTkShift;
-            const uint32_t same = __match_any_sync(0xFFFFFFFFu, take ? bin : 0xFFFFFFFFu);
             if (take) {
               const int64_t slot = t * p.cand_ld + base + __popc(ballot & ((1u << lane) - 1u));
               p.cand_vals[slot] = logit[j];
               p.cand_idx[slot] = (int32_t)(key - st[j]);
-              if (lane == __ffs(same) - 1) atomicAdd(&ts.hist[bin], (uint32_t)__popc(same));
+              // (one atomic per lane: grouping the warp's equal bins with a
+              // match instruction first was slower)
+              atomicAdd(&ts.hist[kk >> kTkShift], 1u);
             }
           }
         } else {

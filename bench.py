@@ -339,29 +339,41 @@ def run_ours(args, rank, world, local_rank):
     h2d = total
     d2h = h_out.numel() * h_out.element_size()
 
-    def e2e_step():
-        d_stage.copy_(h_stage, non_blocking=True)
+    def e2e_step(engine=False):
+        # the copies run on the SMs through the library's idx_copy_async
+        # (engine=True: the same copies by the copy engine, for comparison)
+        if engine:
+            d_stage.copy_(h_stage, non_blocking=True)
+        else:
+            idx.copy_async(d_stage, h_stage)
         idx.quant_insert(d_new_k, d_new_slots, cache)
         idx.quant_q(d_q, out_vals=qv, out_scales=qs)
         idx.paged_logits_topk(qv, qs, d_w, cache, d_bt, d_cl, p.next_n, p.H, TOPK,
                               workspace=ws, out=out)
-        h_out.copy_(out, non_blocking=True)
+        if engine:
+            h_out.copy_(out, non_blocking=True)
+        else:
+            idx.copy_async(h_out, out)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.e2e_steps):
-        flush_l2()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e_mean = reduce_max(sum(e2e_ms) / len(e2e_ms), world, dev)
-    # correctness spot check of the last e2e result against the device result
-    assert torch.equal(h_out, out.cpu())
+    def e2e_time(engine):
+        for _ in range(3):
+            e2e_step(engine)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.e2e_steps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step(engine)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        # correctness spot check of the last e2e result against the device result
+        assert torch.equal(h_out, out.cpu())
+        return reduce_max(sum(ts) / len(ts), world, dev)
+
+    e2e_engine_mean = e2e_time(True)
+    e2e_mean = e2e_time(False)
 
     also = None
     if rank == 0 and not args.no_also:
@@ -410,7 +422,10 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": scored_tokens(p) * world / (e2e_mean * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_mean},
+                "ms_per_step": e2e_mean,
+                "copies": ("one pinned staging buffer in and the indices out per step, each "
+                           "by idx_copy_async (the SMs over NVLink-C2C)"),
+                "ms_per_step_copy_engine": e2e_engine_mean},
         # per timed step: quant_insert, quant_q, the scoring and the select kernels
         "gpu_launches": 4 * K,
         "clocks": clocks.summary(),

@@ -360,6 +360,25 @@ IDX_API idx_status idx_gather_k(const uint8_t* kcache, int64_t num_blocks, int32
                         uint8_t* k_scales, int64_t out_rows, idx_device_errors* errors,
                         idx_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * idx_copy_async -- copy `bytes` bytes from src to dst with the GPU's SMs, for
+ * the small host<->device transfers of a decode step (its inputs in, its top-k
+ * indices out).  The pages have no counterpart for this entry.  On GB300 the
+ * SMs reach page-locked host memory over NVLink-C2C, so for a few hundred KB
+ * this costs about a kernel launch and one memory round trip, less than a
+ * copy-engine transfer.
+ *   dst, src   each either device memory of the current device, managed
+ *              memory, or page-locked host memory mapped into the device's
+ *              address space (as pinned allocations are under unified
+ *              addressing), each covering `bytes` bytes of one allocation;
+ *              the two ranges must not overlap.  Owned by the caller.
+ *   Enqueued on `stream` in stream order (the copy reads src after the
+ *   stream's previous work and later work sees dst); bytes == 0 does nothing.
+ *   A pointer whose first or last byte the device cannot reach is refused
+ *   with IDX_ERR_INVALID_ARG before anything is enqueued.
+ * ------------------------------------------------------------------------ */
+IDX_API idx_status idx_copy_async(void* dst, const void* src, size_t bytes, idx_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

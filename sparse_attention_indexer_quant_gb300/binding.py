@@ -53,6 +53,7 @@ SIGNATURES = {
                                            _P, _SZ, _P, _P]),
     "idx_rope_quant_q": (ctypes.c_int, [_P, _I64, _I32, _P, _P, _P, _I32, _I32, _P, _P, _P, _P]),
     "idx_kpool_insert": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P]),
+    "idx_copy_async": (ctypes.c_int, [_P, _P, _SZ, _P]),
 }
 
 
@@ -405,3 +406,20 @@ def gather_k(kcache, block_table, seq_lens, out_offsets, out_rows: int, errors=N
         _ptr(seq_lens), _ptr(out_offsets), B, _ptr(vals), _ptr(scales), out_rows,
         _ptr(errors), _stream(stream)))
     return vals, scales
+
+
+def copy_async(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copy src into dst (both contiguous, the same number of bytes; each a CUDA
+    tensor of the current device or a pinned CPU tensor) with the GPU's SMs,
+    enqueued on `stream`."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("dst and src must hold the same number of bytes")
+    _check("idx_copy_async", lib.idx_copy_async(_ptr(dst), _ptr(src), n, _stream(stream)))

@@ -23,6 +23,8 @@
 // passes over the row itself, restricted to b1.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "topk_select.cuh"
 
@@ -107,11 +109,12 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
   int n_last = 0;
   const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   // a round: thread t's float4 u covers elements base + 4 * (u * kRowThreads + t) ..+3
-  auto load_round = [&](int64_t base, float4 (&v)[kRowVec]) {
+  auto load_round = [&](int64_t base, float4 (&v)[kRowVec], auto full) {
+    constexpr bool kFull = decltype(full)::value;
 #pragma unroll
     for (int u = 0; u < kRowVec; ++u) {
       const int64_t i0 = base + 4 * ((int64_t)u * kRowThreads + threadIdx.x);
-      if (i0 + 3 < len) {
+      if (kFull || i0 + 3 < len) {
         v[u] = __ldcg(reinterpret_cast<const float4*>(x + i0));
       } else {
         v[u].x = i0 + 0 < len ? __ldcg(x + i0 + 0) : 0.f;
@@ -124,9 +127,11 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
   constexpr int64_t kRound = (int64_t)kRowVec * 4 * kRowThreads;
   if (aligned) {
     constexpr int kVec = kRowVec;
-    for (int64_t base = 0; base < len; base += kRound) {
+    // a round wholly inside the row skips the per-element bounds tests
+    auto hist_round = [&](int64_t base, auto full) {
+      constexpr bool kFull = decltype(full)::value;
       float4 v[kVec];
-      load_round(base, v);
+      load_round(base, v, full);
       // the next round's lines start on their way to L2 while this round's
       // keys are counted (no registers held for them)
 #pragma unroll
@@ -140,12 +145,18 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
         const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (i0 + q < len) {
+          if (kFull || i0 + q < len) {
             const uint32_t key = float_key(e4[q]);
             atomicAdd(&sm.sel.hist[coarse_bin(key)], 1u);
           }
         }
       }
+    };
+    for (int64_t base = 0; base < len; base += kRound) {
+      if (base + kRound <= len)
+        hist_round(base, std::integral_constant<bool, true>());
+      else
+        hist_round(base, std::integral_constant<bool, false>());
     }
     n_last = (int)(len - (int64_t)(n_chunks - 1) * CHUNK);
   } else {
@@ -166,9 +177,10 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
     const uint32_t key_b1 = b1 << kCoarseShift;
     const uint32_t key_gt = key_b1 | ((1u << kCoarseShift) - 1u);
     const int lane = threadIdx.x & 31;
-    for (int64_t base = 0; base < len; base += kRound) {
+    auto classify_round = [&](int64_t base, auto full) {
+      constexpr bool kFull = decltype(full)::value;
       float4 v[kRowVec];
-      load_round(base, v);
+      load_round(base, v, full);
       uint32_t gt = 0u, eq = 0u;
 #pragma unroll
       for (int u = 0; u < kRowVec; ++u) {
@@ -177,7 +189,7 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t key = float_key(e4[q]);
-          const bool in = i0 + q < len;
+          const bool in = kFull || i0 + q < len;
           const uint32_t bit = 1u << (4 * u + q);
           gt |= (key > key_gt && in) ? bit : 0u;
           eq |= ((key ^ key_b1) < (1u << kCoarseShift) && in) ? bit : 0u;
@@ -213,6 +225,12 @@ __device__ __forceinline__ void row_topk(RowTopkSmem<CHUNK>& sm, const float* __
         }
         ++cc;
       }
+    };
+    for (int64_t base = 0; base < len; base += kRound) {
+      if (base + kRound <= len)
+        classify_round(base, std::integral_constant<bool, true>());
+      else
+        classify_round(base, std::integral_constant<bool, false>());
     }
     __syncthreads();
   } else

@@ -305,6 +305,18 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
       st[j] = sStart[half * GH + j];
       en[j] = sEnd[half * GH + j];
     }
+    // the warp's queries' logits rows, and the keys inside every one of their
+    // windows: a tile wholly in there stores without per-query tests
+    float* rows_p[GH];
+    int32_t in_lo = 0, in_hi = 0x7FFFFFFF;
+    const bool all_rows = t0 + half * GH + GH <= p.T;
+#pragma unroll
+    for (int j = 0; j < GH; ++j) {
+      const int64_t t = t0 + half * GH + j;
+      rows_p[j] = p.logits + (t < p.T ? t : 0) * p.ld;
+      in_lo = st[j] > in_lo ? st[j] : in_lo;
+      in_hi = en[j] < in_hi ? en[j] : in_hi;
+    }
     for (int i = 0; i < n_tiles; ++i) {
       if (!mbar_wait(tfull, i & 1, abort)) {
         if (lane == 0) flag_timeout(p.errors, kTimeoutEpilogue);
@@ -324,6 +336,12 @@ __global__ void __launch_bounds__(kMqaThreads, 1)
       const int64_t key = (int64_t)(tile_lo + i) * kTileKeys + m;
       float logit[GH];
       weighted_relu_sum<H, GH>(sW + half * GH * H, d, logit);
+      const int32_t k_tile = (tile_lo + i) * kTileKeys;
+      if (!TOPK && all_rows && k_tile >= in_lo && k_tile + kTileKeys <= in_hi) {
+#pragma unroll
+        for (int j = 0; j < GH; ++j) rows_p[j][k_tile + m] = logit[j];
+        continue;
+      }
 #pragma unroll
       for (int j = 0; j < GH; ++j) {
         const int64_t t = t0 + half * GH + j;
